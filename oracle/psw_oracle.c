@@ -1,0 +1,296 @@
+/*
+ * psw_oracle.c -- plain fp64 CPU oracle for paged sliding-window attention.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this file. It shares no code, header, table or helper
+ * with the CUDA library; the two meet only through the seeded inputs.
+ *
+ * What it computes, and where the pages define it:
+ *
+ *  - Slot mapping: slot = block_table[r][pos / bs] * bs + pos % bs
+ *    ("Gemma 4 model architecture analysis" (vLLM-Kunlun), section 6.3,
+ *    key formula and its worked example; the block table is the page table of
+ *    section 6.2).
+ *  - Cache write (reshape_and_cache): every new token's K row and V row is
+ *    copied to key_cache[block_id, offset, :, :] and value_cache[...], a pool
+ *    laid out [num_blocks, block_size, n_kv_heads, head_dim] (same page,
+ *    section 6.4).
+ *  - Attention for one query at absolute position p of sequence b (the paged
+ *    read of section 6.5; masking and softcap from InfiniLM PR 581
+ *    "feat: support gemma2 and gemma3_text", Gemma-2 item 1 and Gemma-3
+ *    item 3; scale 1.0 from "MNN supports the full Gemma4 family", section
+ *    6.1; GQA grouping from "Gemma 4 architecture decoded", GQA section):
+ *        g   = h / (n_q / n_kv)                    (contiguous GQA groups)
+ *        J   = { j : 0 <= j <= p  and  (W == 0 or p - j < W) }
+ *        s_j = scale * sum_d q_d K_{j,d}
+ *        s_j = cap * tanh(s_j / cap)                (only when cap > 0)
+ *        out = sum_j softmax(s)_j V_j,  lse = log sum_j exp(s_j)
+ *    with V_j = K_j when k_eq_v is set (V aliases the K pages).
+ *    Decode uses p = seq_len - 1 (only the last min(seq_len, W) keys are
+ *    visible); chunked prefill uses p = past + i for chunk row i, which is the
+ *    band rule "key j hidden from query i when past + i - j >= W" composed
+ *    with the aligned causal rule.
+ *  - KV-cache size: batch * seq * layers * n_kv * head_dim * bytes, doubled
+ *    when a separate V cache is kept (the KV-size worked example in
+ *    "Gemma 4 architecture decoded", GQA section).
+ *
+ * Arithmetic: bf16 inputs are widened exactly to double; every sum, the
+ * softcap, the exponentials and the normalisation run in double.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Physical slot of logical position `pos` for one block-table row. */
+int64_t oracle_slot(const int32_t *block_table_row, int64_t pos, int32_t block_size)
+{
+    int64_t logical_block = pos / block_size;
+    int64_t offset = pos % block_size;
+    return (int64_t)block_table_row[logical_block] * block_size + offset;
+}
+
+/* Bytes of KV cache for the given shape; with_v = 0 counts K only. */
+double oracle_kv_cache_bytes(int64_t batch, int64_t seq_len, int64_t n_layers,
+                             int64_t n_kv_heads, int64_t head_dim,
+                             int64_t dtype_bytes, int32_t with_v)
+{
+    double one = (double)batch * (double)seq_len * (double)n_layers *
+                 (double)n_kv_heads * (double)head_dim * (double)dtype_bytes;
+    return with_v ? 2.0 * one : one;
+}
+
+/*
+ * reshape_and_cache: token t of sequence b (t counted from cu_new[b]) sits at
+ * logical position past_lens[b] + (t - cu_new[b]). v_pool may be NULL, in
+ * which case no V row is written (V aliases the K pages).
+ * Returns 0, or -1 when a block id falls outside [0, num_blocks) (nothing is
+ * written for that row).
+ */
+int32_t oracle_kv_cache_write(const uint16_t *k_new, const uint16_t *v_new,
+                              const int32_t *cu_new, const int32_t *past_lens,
+                              int32_t n_seqs, const int32_t *block_table,
+                              int32_t max_blocks_per_seq, int64_t num_blocks,
+                              int32_t n_kv_heads, int32_t head_dim,
+                              int32_t block_size, uint16_t *k_pool,
+                              uint16_t *v_pool)
+{
+    int32_t status = 0;
+    int64_t row_elems = (int64_t)n_kv_heads * head_dim;
+    for (int32_t b = 0; b < n_seqs; ++b) {
+        const int32_t *row = block_table + (int64_t)b * max_blocks_per_seq;
+        for (int32_t t = cu_new[b]; t < cu_new[b + 1]; ++t) {
+            int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]);
+            int64_t slot = oracle_slot(row, pos, block_size);
+            int64_t block_id = slot / block_size;
+            if (block_id < 0 || block_id >= num_blocks) {
+                status = -1;
+                continue;
+            }
+            memcpy(k_pool + slot * row_elems, k_new + (int64_t)t * row_elems,
+                   (size_t)row_elems * sizeof(uint16_t));
+            if (v_pool != NULL)
+                memcpy(v_pool + slot * row_elems, v_new + (int64_t)t * row_elems,
+                       (size_t)row_elems * sizeof(uint16_t));
+        }
+    }
+    return status;
+}
+
+typedef struct {
+    /* layer */
+    int32_t n_q_heads, n_kv_heads, head_dim, window, block_size, k_eq_v;
+    double softcap, scale;
+    /* inputs */
+    const uint16_t *q_rows;   /* [n_rows, n_q_heads, head_dim] */
+    const int32_t *row_seq;   /* [n_rows] */
+    const int64_t *row_pos;   /* [n_rows]; < 0 means an empty row */
+    int64_t n_rows;
+    const uint16_t *k_pool, *v_pool;
+    const int32_t *block_table;
+    int32_t max_blocks_per_seq;
+    /* outputs */
+    double *out;              /* [n_rows, n_q_heads, head_dim] */
+    double *lse;              /* [n_rows, n_q_heads] */
+    /* work split */
+    int32_t n_threads;
+    int32_t thread_index;
+} attn_job_t;
+
+static void attend_one(const attn_job_t *job, int64_t row, int32_t h,
+                       double *scores, double *acc)
+{
+    const int32_t hd = job->head_dim;
+    const int32_t group = job->n_q_heads / job->n_kv_heads;
+    const int32_t g = h / group;
+    const int64_t p = job->row_pos[row];
+    const int32_t *bt_row =
+        job->block_table + (int64_t)job->row_seq[row] * job->max_blocks_per_seq;
+    const uint16_t *q = job->q_rows + (row * job->n_q_heads + h) * (int64_t)hd;
+    const uint16_t *v_pool = job->k_eq_v ? job->k_pool : job->v_pool;
+    double *out = job->out + (row * job->n_q_heads + h) * (int64_t)hd;
+
+    for (int32_t d = 0; d < hd; ++d)
+        out[d] = 0.0;
+    if (p < 0) { /* no keys at all: zero output, lse = -inf */
+        job->lse[row * job->n_q_heads + h] = -INFINITY;
+        return;
+    }
+
+    /* scores over every position 0..p, visibility decided per key */
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= p; ++j) {
+        int visible = (job->window == 0) || (p - j < job->window);
+        if (!visible) {
+            scores[j] = NAN; /* never read */
+            continue;
+        }
+        int64_t slot = oracle_slot(bt_row, j, job->block_size);
+        const uint16_t *k = job->k_pool + (slot * job->n_kv_heads + g) * (int64_t)hd;
+        double dot = 0.0;
+        for (int32_t d = 0; d < hd; ++d)
+            dot += bf16_bits_to_double(q[d]) * bf16_bits_to_double(k[d]);
+        double s = job->scale * dot;
+        if (job->softcap > 0.0)
+            s = job->softcap * tanh(s / job->softcap);
+        scores[j] = s;
+        if (s > m)
+            m = s;
+    }
+
+    double l = 0.0;
+    for (int32_t d = 0; d < hd; ++d)
+        acc[d] = 0.0;
+    for (int64_t j = 0; j <= p; ++j) {
+        int visible = (job->window == 0) || (p - j < job->window);
+        if (!visible)
+            continue;
+        double w = exp(scores[j] - m);
+        l += w;
+        int64_t slot = oracle_slot(bt_row, j, job->block_size);
+        const uint16_t *v = v_pool + (slot * job->n_kv_heads + g) * (int64_t)hd;
+        for (int32_t d = 0; d < hd; ++d)
+            acc[d] += w * bf16_bits_to_double(v[d]);
+    }
+    for (int32_t d = 0; d < hd; ++d)
+        out[d] = acc[d] / l;
+    job->lse[row * job->n_q_heads + h] = m + log(l);
+}
+
+static void *attn_worker(void *arg)
+{
+    const attn_job_t *job = (const attn_job_t *)arg;
+    int64_t max_pos = 0;
+    for (int64_t r = 0; r < job->n_rows; ++r)
+        if (job->row_pos[r] > max_pos)
+            max_pos = job->row_pos[r];
+    double *scores = (double *)malloc((size_t)(max_pos + 1) * sizeof(double));
+    double *acc = (double *)malloc((size_t)job->head_dim * sizeof(double));
+    if (scores == NULL || acc == NULL) {
+        free(scores);
+        free(acc);
+        return (void *)1;
+    }
+    int64_t n_pairs = job->n_rows * job->n_q_heads;
+    for (int64_t pair = job->thread_index; pair < n_pairs; pair += job->n_threads)
+        attend_one(job, pair / job->n_q_heads, (int32_t)(pair % job->n_q_heads),
+                   scores, acc);
+    free(scores);
+    free(acc);
+    return NULL;
+}
+
+int32_t oracle_num_cores(void)
+{
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int32_t)n : 1;
+}
+
+/*
+ * Attention for an arbitrary list of query rows over the paged pools.
+ * Returns the number of threads used, or a negative value on bad arguments
+ * or allocation failure.
+ */
+int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t head_dim, int32_t window, double softcap,
+                              double scale, int32_t k_eq_v, int32_t block_size,
+                              const uint16_t *q_rows, const int32_t *row_seq,
+                              const int64_t *row_pos, int64_t n_rows,
+                              const uint16_t *k_pool, const uint16_t *v_pool,
+                              const int32_t *block_table,
+                              int32_t max_blocks_per_seq, double *out,
+                              double *lse, int32_t n_threads)
+{
+    if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0 ||
+        head_dim <= 0 || window < 0 || softcap < 0.0 || block_size <= 0)
+        return -1;
+    if (!k_eq_v && v_pool == NULL)
+        return -1;
+    if (n_threads <= 0)
+        n_threads = oracle_num_cores();
+    if (n_rows * n_q_heads < n_threads)
+        n_threads = (int32_t)(n_rows * n_q_heads > 0 ? n_rows * n_q_heads : 1);
+
+    attn_job_t *jobs = (attn_job_t *)calloc((size_t)n_threads, sizeof(attn_job_t));
+    pthread_t *threads = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    if (jobs == NULL || threads == NULL) {
+        free(jobs);
+        free(threads);
+        return -2;
+    }
+    int32_t failed = 0;
+    for (int32_t t = 0; t < n_threads; ++t) {
+        attn_job_t *j = &jobs[t];
+        j->n_q_heads = n_q_heads;
+        j->n_kv_heads = n_kv_heads;
+        j->head_dim = head_dim;
+        j->window = window;
+        j->block_size = block_size;
+        j->k_eq_v = k_eq_v;
+        j->softcap = softcap;
+        j->scale = scale;
+        j->q_rows = q_rows;
+        j->row_seq = row_seq;
+        j->row_pos = row_pos;
+        j->n_rows = n_rows;
+        j->k_pool = k_pool;
+        j->v_pool = v_pool;
+        j->block_table = block_table;
+        j->max_blocks_per_seq = max_blocks_per_seq;
+        j->out = out;
+        j->lse = lse;
+        j->n_threads = n_threads;
+        j->thread_index = t;
+    }
+    int32_t started = 0;
+    for (int32_t t = 1; t < n_threads; ++t) {
+        if (pthread_create(&threads[t], NULL, attn_worker, &jobs[t]) != 0)
+            break;
+        started = t;
+    }
+    /* threads that failed to start are run inline */
+    for (int32_t t = started + 1; t < n_threads; ++t)
+        if (attn_worker(&jobs[t]) != NULL)
+            failed = 1;
+    if (attn_worker(&jobs[0]) != NULL)
+        failed = 1;
+    for (int32_t t = 1; t <= started; ++t) {
+        void *ret = NULL;
+        pthread_join(threads[t], &ret);
+        if (ret != NULL)
+            failed = 1;
+    }
+    free(jobs);
+    free(threads);
+    return failed ? -2 : n_threads;
+}
