@@ -1,0 +1,369 @@
+#!/usr/bin/env python
+"""Benchmark of the paged sliding-window attention hot path on one GB300.
+
+One step = the serving step of one sliding attention layer over the
+sliding-layer decode batch (64 sequences, lengths uniform in [512, 4096],
+head_dim 256, 16 query / 8 KV heads, window 1024, 16-token pages in a pool of
+32768 blocks): kv_cache_write of the step's new K/V rows, then
+attn_decode_paged (device plan, split-KV kernel, LSE merge).
+
+Metric: decode attention KV-read GB/s = algorithmic K+V bytes the step must
+read (sum over sequences of min(len, W) keys x n_kv x head_dim x 2 B x 2)
+divided by the step time. Inputs are resident in HBM when the timed region
+starts and are larger than L2 (0.50 GB of KV per step against 129 MB).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica (seed offset by rank)
+on its own GPU; value = bytes of all ranks / max time over ranks.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from paged_sliding_window_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode attn KV-read GB/s (% of HBM peak)"
+UNIT = "GB/s"
+WORKLOAD = "sliding-layer decode batch"
+PROFILE = os.path.join(ROOT, "profiles", "decode_split_sliding_decode_batch.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_sliding_window_gb300", "csrc", f)
+                  for f in ("decode.cu", "ptx.cuh")]
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kv_bytes(step: wl.Step) -> int:
+    """Algorithmic K+V bytes a decode launch must read."""
+    L = step.layer
+    lens = step.seq_lens.astype(np.int64)
+    keys = np.minimum(lens, L.window) if L.window > 0 else lens
+    per_key = L.n_kv_heads * L.head_dim * 2 * (1 if L.k_eq_v else 2)
+    return int(keys.sum()) * per_key
+
+
+def io_bytes(step: wl.Step) -> int:
+    """q in, fp32 out and lse out of a decode launch."""
+    L = step.layer
+    n = step.n_seqs
+    return n * L.n_q_heads * (L.head_dim * 2 + L.head_dim * 4 + 4)
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since it was captured."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_s or m_s.group(1) != source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None):
+    """Times the fp64 oracle on (a subset of) the step; returns
+    (GB/s, threads, description)."""
+    import oracle
+    orc = oracle.default()
+    c = step.cache
+    k0, v0 = c.empty_pools()
+    k1, v1, _ = orc.kv_cache_write(c.hist_k, c.hist_v, c.hist_cu, c.hist_past, step.block_table,
+                                   k0, v0)
+    kp, vp, _ = orc.kv_cache_write(step.new_k, step.new_v, step.cu_new, step.past_lens,
+                                   step.block_table, k1, v1)
+    idx = np.arange(step.n_seqs) if seqs is None else np.asarray(seqs)
+    L = step.layer
+    lens = step.seq_lens[idx].astype(np.int64)
+    keys = np.minimum(lens, L.window) if L.window > 0 else lens
+    nbytes = int(keys.sum()) * L.n_kv_heads * L.head_dim * 2 * (1 if L.k_eq_v else 2)
+    passes, t_total, threads = 0, 0.0, 0
+    while passes == 0 or t_total < budget_s:
+        t0 = time.perf_counter()
+        _, _, threads = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table, step.seq_lens,
+                                   seqs=idx)
+        t_total += time.perf_counter() - t0
+        passes += 1
+    gbs = nbytes * passes / t_total / 1e9
+    desc = (f"fp64 C oracle, {len(idx)} of {step.n_seqs} sequences x all heads, "
+            f"{passes} passes in {t_total:.1f} s")
+    return gbs, threads, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    step = wl.sliding_decode().steps[0]
+    import oracle
+    orc = oracle.default()
+    c = step.cache
+    k0, v0 = c.empty_pools()
+    k1, v1, _ = orc.kv_cache_write(c.hist_k, c.hist_v, c.hist_cu, c.hist_past, step.block_table,
+                                   k0, v0)
+    kp, vp, _ = orc.kv_cache_write(step.new_k, step.new_v, step.cu_new, step.past_lens,
+                                   step.block_table, k1, v1)
+    L = step.layer
+    sample = np.arange(0, step.n_seqs, 4)  # 16 of 64 sequences per step
+    lens = step.seq_lens[sample].astype(np.int64)
+    nbytes = int(np.minimum(lens, L.window).sum()) * L.n_kv_heads * L.head_dim * 4
+    threads = 0
+    for _ in range(args.warmup):
+        orc.decode(L.as_dict(), step.q, kp, vp, step.block_table, step.seq_lens, seqs=sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _, _, threads = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table,
+                                   step.seq_lens, seqs=sample)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    desc = f"fp64 C oracle, {len(sample)} of 64 sequences x all 16 heads per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(step),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(step: wl.Step) -> dict:
+    L = step.layer
+    return {"workload": WORKLOAD, "n_seqs": step.n_seqs, "seq_len": "uniform [512, 4096]",
+            "head_dim": L.head_dim, "n_q_heads": L.n_q_heads, "n_kv_heads": L.n_kv_heads,
+            "window": L.window, "block_size": L.block_size,
+            "pool_blocks": step.cache.num_blocks,
+            "kv_bytes_per_step": kv_bytes(step),
+            "l2": "inputs larger than L2 (KV read per step > 129 MB), no flush",
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    from paged_sliding_window_gb300 import binding, build
+    from paged_sliding_window_gb300.staging import GpuStep, dev_bf16, dev_i32
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    build.build()
+    binding.load(build_if_missing=False)
+
+    step = wl.sliding_decode(seed=2 + 1000 * rank).steps[0]
+    g = GpuStep(step)
+    stream = torch.cuda.current_stream()
+    L = step.layer
+    nbytes = kv_bytes(step)
+
+    def one_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        g.write_new()
+        if ev is not None:
+            ev[1].record(stream)
+        g.decode()
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0, "device error flagged during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    write_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+
+    # end to end through the C ABI: pinned host inputs in, result back to host
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_q = pin(step.q.view(np.int16))
+    h_k = pin(step.new_k.view(np.int16))
+    h_v = pin(step.new_v.view(np.int16))
+    h_meta = [pin(step.cu_new.astype(np.int32)), pin(step.past_lens.astype(np.int32)),
+              pin(step.seq_lens.astype(np.int32)), pin(step.block_table)]
+    d_meta = [g.cu_new, g.past, g.seq_lens, g.table]
+    h_out = torch.empty(g.out.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(g.lse.shape, dtype=torch.float32).pin_memory()
+    h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 +
+           sum(t.numel() * 4 for t in h_meta))
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        g.q.view(torch.int16).copy_(h_q, non_blocking=True)
+        g.new_k.view(torch.int16).copy_(h_k, non_blocking=True)
+        g.new_v.view(torch.int16).copy_(h_v, non_blocking=True)
+        for h, d in zip(h_meta, d_meta):
+            d.copy_(h, non_blocking=True)
+        g.write_new()
+        g.decode()
+        h_out.copy_(g.out, non_blocking=True)
+        h_lse.copy_(g.lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e2e_steps = max(args.steps // 2, 5)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    assert binding.get_error() == 0, "device error flagged during the timed steps"
+
+    times = torch.tensor([elapsed_ms, e2e_s], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms, e2e_s = float(times[0]), float(times[1])
+    ms_per_step = elapsed_ms / args.steps
+    value = nbytes * world / (ms_per_step / 1e3) / 1e9
+    e2e_value = nbytes * world / e2e_s / 1e9
+
+    hbm, _, peak_kind = peaks()
+    achieved = (nbytes + io_bytes(step)) / (decode_ms / 1e3) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(step),
+        "roofline": {"bound": "hbm", "kernel": "attn_decode_paged (plan + split + merge)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": traffic},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": 4 * args.steps,
+        "stage_ms": {"kv_cache_write": write_ms, "attn_decode_paged": decode_ms},
+        "clocks": clock_info,
+    }
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget)
+        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * psw.h -- C ABI of the paged sliding-window attention library (libpsw.so).
+ *
+ * Three operations make one serving step of one attention layer of a
+ * Gemma-style hybrid decoder whose KV cache lives in 16-token pages:
+ *
+ *   kv_cache_write        write the step's new K/V rows into their pages
+ *   attn_decode_paged     one query per sequence over its paged keys
+ *   attn_prefill_chunked  a chunk of queries per sequence over its paged keys
+ *
+ * Page layout (vLLM paged attention as described in "Gemma 4 model
+ * architecture analysis" (vLLM-Kunlun), sections 6.2-6.5): a pool is
+ * [num_blocks][block_size = 16][n_kv_heads][head_dim] bf16, row-major. The
+ * block table is int32 [n_seqs][max_blocks_per_seq]; logical position pos of
+ * sequence b lives in slot block_table[b][pos / 16] * 16 + pos % 16.
+ *
+ * Attention (per sequence b, query head h, query at absolute position p):
+ *   g    = h / (n_q_heads / n_kv_heads)                     GQA group
+ *   J    = { j : j <= p and (window == 0 or p - j < window) }
+ *   s_j  = scale * <q, K_j>;  s_j = softcap * tanh(s_j / softcap) if softcap > 0
+ *   out  = sum_j softmax(s)_j V_j;   lse = log sum_j exp(s_j)  (natural log)
+ * with V_j = K_j when k_eq_v (V aliases the K pages). The window rule is the
+ * band rule of InfiniLM PR 581 ("feat: support gemma2 and gemma3_text",
+ * Gemma-3 item 3): key j is hidden from chunk row i when past + i - j >= W,
+ * composed with the aligned causal rule; decode is the row p = seq_len - 1,
+ * which reads only the last min(seq_len, W) keys. The softcap sits on the
+ * scaled score before mask and softmax (same PR, Gemma-2 item 1 and the
+ * softcap section). Scale 1.0 is Gemma 4's (QK-norm; "MNN supports the full
+ * Gemma4 family", section 6.1), 1/sqrt(query_pre_attn_scalar) is Gemma 2's.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must be device memory of the current
+ *    device (or managed memory); the library never copies host buffers.
+ *    Every bf16 tensor pointer (q, k, v, pools) must be 16-byte aligned.
+ *  - The caller owns every buffer: inputs, pools, tables, outputs and the
+ *    workspace. The library allocates and frees nothing.
+ *  - Calls are asynchronous on `stream` (NULL = legacy default stream) and do
+ *    not synchronise the host, so they can be captured in CUDA graphs.
+ *  - Return value: PSW_OK, or a negative PSW_E* code. Argument errors are
+ *    detected on the host before anything is launched; nothing is written
+ *    then. Errors that only the device can see (a block id outside
+ *    [0, num_blocks), a sequence longer than its block-table row, a negative
+ *    length) set bits in a per-device error word read by psw_get_error();
+ *    the kernels skip the offending access and never trap.
+ *  - Requires an sm_103 GPU (GB300); other devices return PSW_EDEVICE.
+ */
+#ifndef PSW_H
+#define PSW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PSW_API __attribute__((visibility("default")))
+#else
+#define PSW_API
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st *psw_stream_t;
+
+/* ---- return codes (host-detected) ---- */
+#define PSW_OK                 0
+#define PSW_ENULL             -1  /* a required pointer is NULL */
+#define PSW_EINVAL_HEADS      -2  /* n_q_heads or n_kv_heads <= 0, or n_q % n_kv != 0 */
+#define PSW_EINVAL_HDIM       -3  /* head_dim not 256 or 512 */
+#define PSW_EINVAL_SOFTCAP    -4  /* softcap negative or not finite */
+#define PSW_EINVAL_WINDOW     -5  /* window negative */
+#define PSW_EINVAL_BLOCKSIZE  -6  /* block_size != 16 */
+#define PSW_EINVAL_KEQV       -7  /* k_eq_v with a V pointer, or V pointer missing */
+#define PSW_EINVAL_SCALE      -8  /* scale <= 0 or not finite */
+#define PSW_EINVAL_NSEQS      -9  /* n_seqs negative */
+#define PSW_EWORKSPACE       -10  /* workspace smaller than psw_workspace_bytes() */
+#define PSW_ECAPACITY        -11  /* max_blocks_per_seq or num_blocks <= 0, or
+                                     max_seq_len > max_blocks_per_seq * 16 */
+#define PSW_EALIGN           -12  /* a bf16 tensor pointer is not 16-byte aligned */
+#define PSW_EDEVICE          -13  /* no usable sm_103 device */
+#define PSW_ELAUNCH          -14  /* a CUDA launch or attribute call failed */
+#define PSW_ETENSORMAP       -15  /* the TMA descriptor for a pool could not be built */
+
+/* ---- device error bits (psw_get_error) ---- */
+#define PSW_DEVERR_BLOCK_ID    1  /* block id outside [0, num_blocks): access skipped */
+#define PSW_DEVERR_CAPACITY    2  /* sequence longer than its block-table row: clamped */
+#define PSW_DEVERR_LENGTH      4  /* negative length or non-monotone offsets: row skipped */
+#define PSW_DEVERR_PIPELINE    8  /* a bounded pipeline wait timed out: tile abandoned */
+
+/* Per-layer attention parameters. */
+typedef struct {
+  int32_t n_q_heads;   /* query heads; n_q_heads % n_kv_heads == 0 */
+  int32_t n_kv_heads;  /* key/value heads of this layer (may differ per layer) */
+  int32_t head_dim;    /* 256 (sliding layers) or 512 (full layers) */
+  int32_t window;      /* 0 = full causal attention; W > 0 = sliding window of W keys */
+  float   softcap;     /* 0 = off; > 0 applies cap * tanh(s / cap) */
+  float   scale;       /* multiplies q.k before the softcap; > 0 */
+  int32_t k_eq_v;      /* 1: V reads the K pages and every V pointer must be NULL */
+  int32_t block_size;  /* tokens per page; must be 16 */
+} psw_layer_t;
+
+/* Page table of one layer (device pointer, shared by all calls of a step). */
+typedef struct {
+  const int32_t *block_table;  /* device int32 [n_seqs][max_blocks_per_seq] */
+  int32_t max_blocks_per_seq;  /* row length of block_table */
+  int64_t num_blocks;          /* blocks in each pool; valid ids are [0, num_blocks) */
+} psw_pages_t;
+
+/*
+ * Workspace bytes that attn_decode_paged and attn_prefill_chunked need for a
+ * batch of up to n_seqs sequences (max_seq_len bounds every seq_len and every
+ * past_len + chunk length). Pure host arithmetic; needs no GPU. The same
+ * workspace may be reused by consecutive calls on one stream.
+ * Returns PSW_OK and writes *bytes, or an argument error.
+ */
+PSW_API int psw_workspace_bytes(const psw_layer_t *layer, int32_t n_seqs, int32_t max_seq_len,
+                        size_t *bytes);
+
+/*
+ * reshape_and_cache ("Gemma 4 model architecture analysis", section 6.4):
+ * token t of sequence b (cu_new[b] <= t < cu_new[b+1]) has logical position
+ * past_lens[b] + (t - cu_new[b]); its K row k[t] (n_kv_heads x head_dim bf16)
+ * is copied bit for bit into that position's slot of k_pool, and v[t] into
+ * v_pool. With k_eq_v, v and v_pool must be NULL and only K is written.
+ *   k, v       device bf16 [n_new_total][n_kv_heads][head_dim], n_new_total = cu_new[n_seqs]
+ *   cu_new     device int32 [n_seqs + 1], non-decreasing, cu_new[0] = 0
+ *   past_lens  device int32 [n_seqs], tokens already cached per sequence
+ *   pages      block table of the pools; it must cover every written position
+ *   k_pool, v_pool  device bf16 [num_blocks][16][n_kv_heads][head_dim], written
+ * Slots whose block id falls outside the pool are skipped and flagged
+ * (PSW_DEVERR_BLOCK_ID); every other slot of the pools is left untouched.
+ */
+PSW_API int kv_cache_write(const psw_layer_t *layer, const void *k, const void *v,
+                   const int32_t *cu_new, const int32_t *past_lens, int32_t n_seqs,
+                   const psw_pages_t *pages, void *k_pool, void *v_pool,
+                   psw_stream_t stream);
+
+/*
+ * Decode attention: sequence b has seq_lens[b] cached tokens, the last of
+ * which is the query's own (write it with kv_cache_write first); its single
+ * query q[b] sits at position seq_lens[b] - 1. Sliding layers read only the
+ * last min(seq_len, window) keys.
+ *   q          device bf16 [n_seqs][n_q_heads][head_dim]
+ *   k_pool     device bf16 pool; v_pool likewise, NULL when k_eq_v
+ *   seq_lens   device int32 [n_seqs]; 0 gives a zero row and lse = -inf
+ *   out        device fp32 [n_seqs][n_q_heads][head_dim]
+ *   lse        device fp32 [n_seqs][n_q_heads] or NULL
+ *   ws         device workspace of ws_bytes >= psw_workspace_bytes(layer, n_seqs, .)
+ * Split-KV flash decoding: partial results over page ranges go to the
+ * workspace and a log-sum-exp merge combines them.
+ */
+PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const void *k_pool,
+                      const void *v_pool, const psw_pages_t *pages,
+                      const int32_t *seq_lens, int32_t n_seqs, float *out, float *lse,
+                      void *ws, size_t ws_bytes, psw_stream_t stream);
+
+/*
+ * Chunked prefill: sequence b contributes the chunk rows
+ * cu_q[b] <= t < cu_q[b+1]; row i = t - cu_q[b] sits at position
+ * past_lens[b] + i and attends over keys [0, past_lens[b] + i] under the band
+ * and causal rules. The chunk's own K/V must already be in the pages
+ * (kv_cache_write first).
+ *   q          device bf16 [n_q_total][n_q_heads][head_dim], n_q_total = cu_q[n_seqs]
+ *   cu_q       device int32 [n_seqs + 1]; past_lens device int32 [n_seqs]
+ *   out        device fp32 [n_q_total][n_q_heads][head_dim]; lse fp32 [n_q_total][n_q_heads] or NULL
+ *   max_q_len  host bound on every chunk length (cu_q[b+1] - cu_q[b])
+ *   ws         as for attn_decode_paged
+ * Tensor-core kernel (tcgen05/TMEM with TMA-fed tiles); key tiles that the
+ * band rule hides from every row of a query tile are never loaded.
+ */
+PSW_API int attn_prefill_chunked(const psw_layer_t *layer, const void *q, const int32_t *cu_q,
+                         const int32_t *past_lens, int32_t n_seqs, int32_t max_q_len,
+                         const void *k_pool, const void *v_pool, const psw_pages_t *pages,
+                         float *out, float *lse, void *ws, size_t ws_bytes,
+                         psw_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the current device's error word (an OR
+ * of PSW_DEVERR_* bits, 0 when nothing was flagged) in *device_error_out and
+ * clears it. Returns PSW_OK or PSW_ELAUNCH when the stream reports an error.
+ */
+PSW_API int psw_get_error(psw_stream_t stream, int32_t *device_error_out);
+
+/* Static string describing a return code. */
+PSW_API const char *psw_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSW_H */

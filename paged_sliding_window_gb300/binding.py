@@ -1,0 +1,195 @@
+"""Thin ctypes binding of libpsw.so (the C ABI declared in include/psw.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU, checks dtypes and shapes, and passes raw pointers, sizes and
+the current CUDA stream to the C entry point of the same name. All arithmetic
+runs in the CUDA kernels of the library; there is no fallback. If the
+library cannot be loaded, every call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PSW_OK = 0
+ERRORS = {
+    -1: "PSW_ENULL", -2: "PSW_EINVAL_HEADS", -3: "PSW_EINVAL_HDIM", -4: "PSW_EINVAL_SOFTCAP",
+    -5: "PSW_EINVAL_WINDOW", -6: "PSW_EINVAL_BLOCKSIZE", -7: "PSW_EINVAL_KEQV",
+    -8: "PSW_EINVAL_SCALE", -9: "PSW_EINVAL_NSEQS", -10: "PSW_EWORKSPACE",
+    -11: "PSW_ECAPACITY", -12: "PSW_EALIGN", -13: "PSW_EDEVICE", -14: "PSW_ELAUNCH",
+    -15: "PSW_ETENSORMAP",
+}
+DEVERR_BLOCK_ID, DEVERR_CAPACITY, DEVERR_LENGTH, DEVERR_PIPELINE = 1, 2, 4, 8
+EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
+            "attn_prefill_chunked", "psw_get_error", "psw_strerror")
+
+
+class PswLayer(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("softcap", ctypes.c_float), ("scale", ctypes.c_float),
+                ("k_eq_v", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+class PswPages(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int64)]
+
+
+class PswError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({strerror(code)})")
+        self.code = code
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Loads libpsw.so (building it first if asked and missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libpsw.so not built ({path})")
+            path = _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lp = ctypes.POINTER(PswLayer)
+        pp = ctypes.POINTER(PswPages)
+        lib.psw_workspace_bytes.argtypes = [lp, i32, i32, ctypes.POINTER(sz)]
+        lib.kv_cache_write.argtypes = [lp, vp, vp, vp, vp, i32, pp, vp, vp, vp]
+        lib.attn_decode_paged.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz, vp]
+        lib.attn_prefill_chunked.argtypes = [lp, vp, vp, vp, i32, i32, vp, vp, pp, vp, vp, vp,
+                                             sz, vp]
+        lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
+        lib.psw_strerror.argtypes = [ctypes.c_int]
+        lib.psw_strerror.restype = ctypes.c_char_p
+        for name in ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
+                     "attn_prefill_chunked", "psw_get_error"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load(build_if_missing=False).psw_strerror(int(code)).decode()
+    except Exception:
+        return ERRORS.get(code, str(code))
+
+
+def make_layer(layer) -> PswLayer:
+    """From any object with the psw_layer_t fields (e.g. workloads.Layer)."""
+    return PswLayer(int(layer.n_q_heads), int(layer.n_kv_heads), int(layer.head_dim),
+                    int(layer.window), float(layer.softcap), float(layer.scale),
+                    int(bool(layer.k_eq_v)), int(getattr(layer, "block_size", 16)))
+
+
+def make_pages(block_table: torch.Tensor, num_blocks: int) -> PswPages:
+    _check(block_table, torch.int32, "block_table")
+    return PswPages(block_table.data_ptr(), int(block_table.shape[1]), int(num_blocks))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(rc, what):
+    if rc != PSW_OK:
+        raise PswError(rc, what)
+
+
+def workspace_bytes(layer, n_seqs: int, max_seq_len: int) -> int:
+    out = ctypes.c_size_t(0)
+    _raise(load().psw_workspace_bytes(ctypes.byref(make_layer(layer)), int(n_seqs),
+                                      int(max_seq_len), ctypes.byref(out)), "psw_workspace_bytes")
+    return int(out.value)
+
+
+def alloc_workspace(layer, n_seqs: int, max_seq_len: int, device="cuda") -> torch.Tensor:
+    """A caller-owned workspace of the size the library asks for."""
+    return torch.empty(max(workspace_bytes(layer, n_seqs, max_seq_len), 256), dtype=torch.uint8,
+                       device=device)
+
+
+def kv_cache_write(layer, k, v, cu_new, past_lens, pages: PswPages, k_pool, v_pool,
+                   stream=None) -> None:
+    for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _check(t, torch.bfloat16, n)
+    _check(cu_new, torch.int32, "cu_new")
+    _check(past_lens, torch.int32, "past_lens")
+    rc = load().kv_cache_write(ctypes.byref(make_layer(layer)), _ptr(k), _ptr(v), _ptr(cu_new),
+                               _ptr(past_lens), int(past_lens.shape[0]), ctypes.byref(pages),
+                               _ptr(k_pool), _ptr(v_pool), _stream(stream))
+    _raise(rc, "kv_cache_write")
+
+
+def attn_decode_paged(layer, q, k_pool, v_pool, pages: PswPages, seq_lens, out, lse=None,
+                      ws=None, stream=None) -> None:
+    _check(q, torch.bfloat16, "q")
+    _check(k_pool, torch.bfloat16, "k_pool")
+    _check(v_pool, torch.bfloat16, "v_pool")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(out, torch.float32, "out")
+    _check(lse, torch.float32, "lse")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().attn_decode_paged(ctypes.byref(make_layer(layer)), _ptr(q), _ptr(k_pool),
+                                  _ptr(v_pool), ctypes.byref(pages), _ptr(seq_lens),
+                                  int(seq_lens.shape[0]), _ptr(out), _ptr(lse), _ptr(ws),
+                                  ws_bytes, _stream(stream))
+    _raise(rc, "attn_decode_paged")
+
+
+def attn_prefill_chunked(layer, q, cu_q, past_lens, max_q_len: int, k_pool, v_pool,
+                         pages: PswPages, out, lse=None, ws=None, stream=None) -> None:
+    _check(q, torch.bfloat16, "q")
+    _check(cu_q, torch.int32, "cu_q")
+    _check(past_lens, torch.int32, "past_lens")
+    _check(k_pool, torch.bfloat16, "k_pool")
+    _check(v_pool, torch.bfloat16, "v_pool")
+    _check(out, torch.float32, "out")
+    _check(lse, torch.float32, "lse")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().attn_prefill_chunked(ctypes.byref(make_layer(layer)), _ptr(q), _ptr(cu_q),
+                                     _ptr(past_lens), int(past_lens.shape[0]), int(max_q_len),
+                                     _ptr(k_pool), _ptr(v_pool), ctypes.byref(pages), _ptr(out),
+                                     _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
+    _raise(rc, "attn_prefill_chunked")
+
+
+def get_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    val = ctypes.c_int32(0)
+    _raise(load().psw_get_error(_stream(stream), ctypes.byref(val)), "psw_get_error")
+    return int(val.value)

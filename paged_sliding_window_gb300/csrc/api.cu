@@ -1,0 +1,289 @@
+// api.cu -- the extern "C" surface of libpsw (include/psw.h): argument
+// validation (every error is returned before anything is launched), TMA
+// descriptors for the page pools, the per-device error word, and dispatch to
+// the kernel launchers.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "psw_internal.h"
+
+namespace psw {
+
+// Device-side error word: kernels OR PSW_DEVERR_* bits into it.
+__device__ int32_t g_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  DeviceInfo info{};
+  int32_t* err = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+DeviceState* current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    DeviceInfo info{};
+    info.device = dev;
+    if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess)
+      return nullptr;
+    void* err = nullptr;
+    if (cudaGetSymbolAddress(&err, g_error_word) != cudaSuccess) return nullptr;
+    st.info = info;
+    st.err = static_cast<int32_t*>(err);
+    st.ready = true;
+  }
+  return &st;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layer(const psw_layer_t* layer, LayerArgs* out) {
+  if (layer == nullptr) return PSW_ENULL;
+  if (layer->n_q_heads <= 0 || layer->n_kv_heads <= 0 ||
+      layer->n_q_heads % layer->n_kv_heads != 0)
+    return PSW_EINVAL_HEADS;
+  if (layer->head_dim != 256 && layer->head_dim != 512) return PSW_EINVAL_HDIM;
+  if (!(layer->softcap >= 0.f) || !isfinite(layer->softcap)) return PSW_EINVAL_SOFTCAP;
+  if (layer->window < 0) return PSW_EINVAL_WINDOW;
+  if (layer->block_size != kBlockSize) return PSW_EINVAL_BLOCKSIZE;
+  if (!(layer->scale > 0.f) || !isfinite(layer->scale)) return PSW_EINVAL_SCALE;
+  if (layer->k_eq_v != 0 && layer->k_eq_v != 1) return PSW_EINVAL_KEQV;
+  out->n_q = layer->n_q_heads;
+  out->n_kv = layer->n_kv_heads;
+  out->hd = layer->head_dim;
+  out->window = layer->window;
+  out->softcap = layer->softcap;
+  out->scale = layer->scale;
+  out->k_eq_v = layer->k_eq_v != 0;
+  return PSW_OK;
+}
+
+int check_pages(const psw_pages_t* pages) {
+  if (pages == nullptr || pages->block_table == nullptr) return PSW_ENULL;
+  if (pages->max_blocks_per_seq <= 0 || pages->num_blocks <= 0) return PSW_ECAPACITY;
+  // block ids are int32 and TMA slot coordinates (id * 16) must fit int32
+  if (pages->num_blocks > (int64_t{1} << 27)) return PSW_ECAPACITY;
+  if (static_cast<int64_t>(pages->max_blocks_per_seq) * kBlockSize > INT32_MAX)
+    return PSW_ECAPACITY;
+  return PSW_OK;
+}
+
+// k_eq_v: V must be absent; otherwise present.
+int check_v(const LayerArgs& L, const void* v_ptr) {
+  if (L.k_eq_v && v_ptr != nullptr) return PSW_EINVAL_KEQV;
+  if (!L.k_eq_v && v_ptr == nullptr) return PSW_EINVAL_KEQV;
+  return PSW_OK;
+}
+
+int device_ready(DeviceState** st) {
+  *st = current_device();
+  if (*st == nullptr) return PSW_EDEVICE;
+  if ((*st)->info.cc_major != 10 || (*st)->info.cc_minor != 3) return PSW_EDEVICE;
+  return PSW_OK;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* info) {
+  DeviceState* st = current_device();
+  if (st == nullptr) return cudaErrorNoDevice;
+  *info = st->info;
+  return cudaSuccess;
+}
+
+int32_t* device_error_word() {
+  DeviceState* st = current_device();
+  return st ? st->err : nullptr;
+}
+
+int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
+                         int hd) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return PSW_ETENSORMAP;
+  // [slot][chunk of 64 elements across (kv head, head_dim)][64 elements]
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_kv) * (hd / 64),
+                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(n_kv) * hd * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
+}
+
+}  // namespace psw
+
+using namespace psw;
+
+extern "C" {
+
+int psw_workspace_bytes(const psw_layer_t* layer, int32_t n_seqs, int32_t max_seq_len,
+                        size_t* bytes) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (bytes == nullptr) return PSW_ENULL;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (max_seq_len < 0) return PSW_ECAPACITY;
+  *bytes = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total;
+  return PSW_OK;
+}
+
+int kv_cache_write(const psw_layer_t* layer, const void* k, const void* v,
+                   const int32_t* cu_new, const int32_t* past_lens, int32_t n_seqs,
+                   const psw_pages_t* pages, void* k_pool, void* v_pool, psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (k == nullptr || cu_new == nullptr || past_lens == nullptr || k_pool == nullptr)
+    return PSW_ENULL;
+  if ((rc = check_v(L, v)) != PSW_OK) return rc;
+  if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
+  if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+    return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  cudaError_t e = launch_kv_cache_write(L, k, v, cu_new, past_lens, n_seqs, pages->block_table,
+                                        pages->max_blocks_per_seq, pages->num_blocks, k_pool,
+                                        v_pool, st->info.num_sms, st->err,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
+}
+
+int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_pool,
+                      const void* v_pool, const psw_pages_t* pages, const int32_t* seq_lens,
+                      int32_t n_seqs, float* out, float* lse, void* ws, size_t ws_bytes,
+                      psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (q == nullptr || k_pool == nullptr || seq_lens == nullptr || out == nullptr)
+    return PSW_ENULL;
+  if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
+  if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  if (ws == nullptr) return PSW_EWORKSPACE;
+  if (ws_bytes < decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total) return PSW_EWORKSPACE;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  CUtensorMap k_map, v_map;
+  if ((rc = make_pool_tensor_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd)) != PSW_OK)
+    return rc;
+  if (L.k_eq_v) {
+    v_map = k_map;
+  } else if ((rc = make_pool_tensor_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd)) !=
+             PSW_OK) {
+    return rc;
+  }
+  return launch_decode(L, q, k_map, v_map, pages->block_table, pages->max_blocks_per_seq,
+                       pages->num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
+                       st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t* cu_q,
+                         const int32_t* past_lens, int32_t n_seqs, int32_t max_q_len,
+                         const void* k_pool, const void* v_pool, const psw_pages_t* pages,
+                         float* out, float* lse, void* ws, size_t ws_bytes,
+                         psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (q == nullptr || cu_q == nullptr || past_lens == nullptr || k_pool == nullptr ||
+      out == nullptr)
+    return PSW_ENULL;
+  if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
+  if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (max_q_len < 0) return PSW_ECAPACITY;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PSW_EALIGN;
+  (void)ws;
+  (void)ws_bytes;
+  (void)stream;
+  (void)lse;
+  if (n_seqs == 0 || max_q_len == 0) return PSW_OK;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  return PSW_ELAUNCH;  // prefill kernel not built yet
+}
+
+int psw_get_error(psw_stream_t stream, int32_t* device_error_out) {
+  if (device_error_out == nullptr) return PSW_ENULL;
+  DeviceState* st = current_device();
+  if (st == nullptr) return PSW_EDEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PSW_ELAUNCH;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, st->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PSW_ELAUNCH;
+  const int32_t zero = 0;
+  if (cudaMemcpy(st->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PSW_ELAUNCH;
+  *device_error_out = v;
+  return PSW_OK;
+}
+
+const char* psw_strerror(int code) {
+  switch (code) {
+    case PSW_OK: return "ok";
+    case PSW_ENULL: return "a required pointer is NULL";
+    case PSW_EINVAL_HEADS: return "n_q_heads must be a positive multiple of n_kv_heads";
+    case PSW_EINVAL_HDIM: return "head_dim must be 256 or 512";
+    case PSW_EINVAL_SOFTCAP: return "softcap must be finite and >= 0 (0 = off)";
+    case PSW_EINVAL_WINDOW: return "window must be >= 0 (0 = full attention)";
+    case PSW_EINVAL_BLOCKSIZE: return "block_size must be 16";
+    case PSW_EINVAL_KEQV: return "k_eq_v requires NULL V pointers; otherwise V is required";
+    case PSW_EINVAL_SCALE: return "scale must be finite and > 0";
+    case PSW_EINVAL_NSEQS: return "n_seqs must be >= 0";
+    case PSW_EWORKSPACE: return "workspace is missing or smaller than psw_workspace_bytes()";
+    case PSW_ECAPACITY: return "page table capacity out of range";
+    case PSW_EALIGN: return "bf16 tensors must be 16-byte aligned";
+    case PSW_EDEVICE: return "no usable sm_103 (GB300) device";
+    case PSW_ELAUNCH: return "CUDA launch failed";
+    case PSW_ETENSORMAP: return "could not build the TMA descriptor of a pool";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

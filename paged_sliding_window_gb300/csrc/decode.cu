@@ -1,0 +1,651 @@
+// decode.cu -- split-KV flash decoding over 16-token pages.
+//
+// Method (what is computed): for each sequence b and query head h, the single
+// query at position p = seq_len - 1 attends over keys j <= p that the sliding
+// window leaves visible (p - j < W, i.e. only the last min(seq_len, W) keys:
+// InfiniLM PR 581 "feat: support gemma2 and gemma3_text", Gemma-3 item 3),
+// with s = scale * q.k, the optional softcap cap * tanh(s / cap) on the scaled
+// score before the softmax (same PR, Gemma-2 item 1), and V read from the K
+// pages when k_eq_v ("MNN supports the full Gemma4 family", section 6.2).
+// Keys are fetched through the block table of "Gemma 4 model architecture
+// analysis" (vLLM-Kunlun), sections 6.3 and 6.5.
+//
+// Design (how, on sm_103a):
+//  * Work unit = (sequence, KV head, group of <= 8 query heads); a unit's
+//    visible pages are cut into tiles of 4 pages (64 keys). All tiles of all
+//    units form one list, planned on the device from seq_lens, and a
+//    persistent grid (one CTA per SM) takes equal contiguous slices of it, so
+//    the load is balanced whatever the length mix.
+//  * Warp 4 is the producer: it reads block ids and issues one 2 KB TMA box
+//    per (page, 128-byte chunk of head_dim) into a 3-stage shared-memory ring
+//    (128-byte swizzle), completing on mbarriers.
+//  * Warps 0-3 consume. Each owns a quarter of head_dim. QK: mma.sync
+//    m16n8k16 with 16 keys as M and the query group as N (S^T = K Q^T), partial
+//    over the warp's quarter; the four partials meet in shared memory (one
+//    named barrier per tile), every warp forms the full scores of the tile,
+//    runs the online softmax in fp32 (exp2 domain) and splits P into a bf16
+//    high part and a bf16 remainder, both used as the B operand of PV:
+//    O^T[d, h] += V^T[d, key] (P_hi + P_lo)^T[key, h] over its quarter.
+//  * A unit whose tiles all fall in one CTA writes its normalised output
+//    directly; units cut by a slice boundary leave (m, l, O) partials in the
+//    workspace (slot = CTA + unit, which is unique because slices and units
+//    are both contiguous in tile order) and a merge kernel combines them with
+//    the log-sum-exp rule.
+//  * Rows of a partially visible page (before the window start or past the
+//    end) are masked in the scores and their V rows zeroed in shared memory,
+//    so stale or non-finite cache contents never reach the output.
+#include <math.h>
+
+#include "psw_internal.h"
+#include "ptx.cuh"
+
+namespace psw {
+namespace dec {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kChunkBytes = kBlockSize * 128;  // one TMA box: 16 rows x 128 B
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct SeqPlan {
+  int32_t tile_off;  // first tile of this sequence in the global tile list
+  int32_t len;       // seq_len after validation
+  int32_t lo;        // first visible position
+  int32_t ntu;       // tiles per unit
+};
+
+template <int HD, bool KEQV>
+struct Cfg {
+  static constexpr int kChunks = HD / 64;
+  static constexpr int kPageBytes = kChunks * kChunkBytes;
+  static constexpr int kTilePages = (HD == 512 && !KEQV) ? 2 : 4;
+  static constexpr int kTileKeys = kTilePages * kBlockSize;
+  static constexpr int kKTileBytes = kTilePages * kPageBytes;
+  static constexpr int kStageBytes = kKTileBytes * (KEQV ? 1 : 2);
+  static constexpr int kStagesFit = 196608 / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kDPerWarp = HD / kConsumerWarps;
+  static constexpr int kKSteps = kDPerWarp / 16;
+  static constexpr int kMTiles = kDPerWarp / 16;
+  static constexpr int kChunksPerWarp = kDPerWarp / 64;
+  static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kTileKeys;
+  static constexpr int kTmaPerTile = kTilePages * kChunks * (KEQV ? 1 : 2);
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + 32;
+  static_assert(kTmaPerTile <= 32, "one TMA box per producer lane");
+  static_assert(kStages >= 2, "need a pipeline");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+// XOR swizzle of the key index in the score-exchange buffer: conflict-free
+// for both the fragment-layout writes and the row-wise float2 reads.
+__device__ __forceinline__ int sbuf_key(int qh, int key) {
+  return key ^ (((qh ^ (qh >> 2)) & 3) << 3);
+}
+
+// ---------------------------------------------------------------- plan
+// One CTA: validates seq_lens, computes per-sequence tile counts and their
+// exclusive prefix. plan[n_seqs].tile_off holds the total.
+__global__ void __launch_bounds__(1024)
+decode_plan_kernel(const int32_t* __restrict__ seq_lens, int n_seqs, int window,
+                   int max_blocks, int units_per_seq, int tile_pages,
+                   SeqPlan* __restrict__ plan, int32_t* err) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int cap = max_blocks * kBlockSize;
+  for (int base = 0; base < n_seqs; base += blockDim.x) {
+    const int s = base + tid;
+    int len = 0, lo = 0, ntu = 0;
+    if (s < n_seqs) {
+      len = seq_lens[s];
+      if (len < 0) { flag_error(err, PSW_DEVERR_LENGTH); len = 0; }
+      if (len > cap) { flag_error(err, PSW_DEVERR_CAPACITY); len = cap; }
+      lo = (window > 0 && len > window) ? len - window : 0;
+      if (len > 0) {
+        const int npages = (len - 1) / kBlockSize - lo / kBlockSize + 1;
+        ntu = (npages + tile_pages - 1) / tile_pages;
+      }
+    }
+    const int tiles = ntu * units_per_seq;
+    int incl = tiles;
+    #pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x >> 5;
+      int w = lane < nw ? warp_tot[lane] : 0;
+      #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += v;
+      }
+      warp_tot[lane] = w;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int excl = incl - tiles + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (s < n_seqs) plan[s] = SeqPlan{carry + excl, len, lo, ntu};
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[(blockDim.x >> 5) - 1];
+    __syncthreads();
+  }
+  if (tid == 0) plan[n_seqs] = SeqPlan{carry, 0, 0, 0};
+}
+
+// ---------------------------------------------------------------- walker
+// Iterates the global tile list in order: sequence, unit, tile.
+struct Walker {
+  const SeqPlan* plan;
+  int n_seqs, ups;
+  int s, unit, tile;
+  int ntu, len, lo, tile_off;
+
+  __device__ void load_seq() {
+    const SeqPlan p = plan[s];
+    tile_off = p.tile_off; len = p.len; lo = p.lo; ntu = p.ntu;
+  }
+  __device__ void init(const SeqPlan* pl, int ns, int u, int t) {
+    plan = pl; n_seqs = ns; ups = u;
+    int a = 0, b = ns;  // plan[a].tile_off <= t < plan[b].tile_off
+    while (b - a > 1) {
+      const int mid = (a + b) >> 1;
+      if (plan[mid].tile_off <= t) a = mid; else b = mid;
+    }
+    s = a;
+    load_seq();
+    const int rem = t - tile_off;
+    unit = rem / ntu;
+    tile = rem - unit * ntu;
+  }
+  __device__ void advance() {
+    if (++tile < ntu) return;
+    tile = 0;
+    if (++unit < ups) return;
+    unit = 0;
+    do { ++s; } while (s < n_seqs && plan[s + 1].tile_off == plan[s].tile_off);
+    if (s < n_seqs) load_seq();
+  }
+  __device__ int first_page() const { return lo / kBlockSize; }
+  __device__ int last_page() const { return (len - 1) / kBlockSize; }
+  __device__ int unit_first_tile() const { return tile_off + unit * ntu; }
+  __device__ int global_unit() const { return s * ups + unit; }
+};
+
+// ---------------------------------------------------------------- split
+template <int HD, bool KEQV>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map,
+                    const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
+                    int max_blocks, int64_t num_blocks, const SeqPlan* __restrict__ plan,
+                    int n_seqs, int n_q, int n_kv, int group, int qchunks, float scale,
+                    float softcap, float* __restrict__ out, float* __restrict__ lse,
+                    float* __restrict__ ws_o, float2* __restrict__ ws_ml, int32_t* err) {
+  using C = Cfg<HD, KEQV>;
+  constexpr int TP = C::kTilePages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  float* sbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sbuf + 2 * C::kSBufFloats);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + C::kStages);
+  volatile int* cons_abort = abort_flag + 1;  // written only by consumer warps
+
+  const int ups = n_kv * qchunks;
+  const int total = plan[n_seqs].tile_off;
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int t_begin = blockIdx.x * per;
+  const int t_end = min(total, t_begin + per);
+  if (t_begin >= t_end) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    *cons_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&k_map);
+      if (!KEQV) prefetch_tensormap(&v_map);
+    }
+    const uint64_t policy = l2_policy_evict_first();
+    Walker w;
+    w.init(plan, n_seqs, ups, t_begin);
+    // lane -> (K/V, page in tile, chunk) of its TMA box
+    const int which = lane / (TP * C::kChunks);
+    const int lp = (lane % (TP * C::kChunks)) / C::kChunks;
+    const int lc = lane % C::kChunks;
+    int issued = 0;
+    for (int t = t_begin; t < t_end; ++t, ++issued) {
+      const int stage = issued % C::kStages;
+      const uint32_t ph = (issued / C::kStages) & 1;
+      const int kvh = w.unit / qchunks;
+      const int page0 = w.first_page() + w.tile * TP;
+      const int npages = min(TP, w.last_page() - page0 + 1);
+      int blk = -1;
+      if (lane < npages) {
+        blk = block_table[static_cast<int64_t>(w.s) * max_blocks + page0 + lane];
+        if (blk < 0 || blk >= num_blocks) {
+          flag_error(err, PSW_DEVERR_BLOCK_ID);
+          blk = -1;  // out-of-range box: TMA fills zeros
+        }
+      }
+      const int my_blk = __shfl_sync(0xffffffffu, blk, lp);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&empty_bar[stage], ph ^ 1);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || *abort_flag) {
+        if (lane == 0) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
+        break;
+      }
+      if (lane == 0)
+        mbar_arrive_expect_tx(&full_bar[stage],
+                              static_cast<uint32_t>(npages * C::kPageBytes * (KEQV ? 1 : 2)));
+      __syncwarp();
+      if (lane < C::kTmaPerTile && lp < npages) {
+        uint8_t* dst = stages + stage * C::kStageBytes + which * C::kKTileBytes +
+                       lp * C::kPageBytes + lc * kChunkBytes;
+        const CUtensorMap* map = (which == 0) ? &k_map : &v_map;
+        tma_load_3d_hint(dst, map, &full_bar[stage], 0, kvh * C::kChunks + lc,
+                         my_blk * kBlockSize, policy);
+      }
+      w.advance();
+    }
+    // drain: the last phase of every stage used must have landed before exit
+    if (lane == 0) {
+      for (int i = max(0, issued - C::kStages); i < issued; ++i)
+        mbar_wait(&full_bar[i % C::kStages], (i / C::kStages) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, t4 = lane & 3;
+  const float scale_l2 = scale * kLog2e;
+  const bool use_cap = softcap > 0.f;
+  float o[C::kMTiles][4];
+  uint32_t qf[C::kKSteps][2];
+  float m_run = -INFINITY, l_run = 0.f;
+  int nh = 0, hb = 0;
+
+  // per-lane ldmatrix geometry
+  const int j8 = lane >> 3, r8 = lane & 7;
+  const int qk_row = (j8 & 1) * 8 + r8;       // key row within a page (QK, A = K)
+  const int qk_unit_add = j8 >> 1;            // +8 columns of d
+  const int pv_row = (j8 >> 1) * 8 + r8;      // key row within a page (PV, A = V^T)
+  const int pv_dadd = (j8 & 1) * 8;
+  const uint32_t stages_u32 = smem_u32(stages);
+
+  Walker w;
+  w.init(plan, n_seqs, ups, t_begin);
+  int consumed = 0;
+  for (int t = t_begin; t < t_end; ++t, ++consumed) {
+    const int stage = consumed % C::kStages;
+    const uint32_t ph = (consumed / C::kStages) & 1;
+    const bool unit_start = (w.tile == 0) || (t == t_begin);
+    if (unit_start) {
+      const int kvh = w.unit / qchunks, qc = w.unit - (w.unit / qchunks) * qchunks;
+      hb = kvh * group + qc * kQHeadsPerUnit;
+      nh = min(kQHeadsPerUnit, group - qc * kQHeadsPerUnit);
+      const __nv_bfloat16* qrow =
+          q + (static_cast<int64_t>(w.s) * n_q + hb + g) * HD + warp * C::kDPerWarp + t4 * 2;
+      #pragma unroll
+      for (int ks = 0; ks < C::kKSteps; ++ks) {
+        if (g < nh) {
+          qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16);
+          qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8);
+        } else {
+          qf[ks][0] = 0u;
+          qf[ks][1] = 0u;
+        }
+      }
+      #pragma unroll
+      for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    const int page0 = w.first_page() + w.tile * TP;
+    const int npages = min(TP, w.last_page() - page0 + 1);
+    const int pos0 = page0 * kBlockSize;
+
+    // A timed-out wait is decided collectively after the named barrier below,
+    // so that all consumer warps pass the same number of barriers.
+    const bool landed = mbar_wait(&full_bar[stage], ph);
+    if (!landed && lane == 0) {
+      flag_error(err, PSW_DEVERR_PIPELINE);
+      *cons_abort = 1;
+    }
+    const uint32_t kbase = stages_u32 + stage * C::kStageBytes;
+    const uint32_t vbase = KEQV ? kbase : kbase + C::kKTileBytes;
+
+    // ---- QK over this warp's quarter of head_dim: S^T[key, qh]
+    float sacc[TP][4];
+    #pragma unroll
+    for (int mt = 0; mt < TP; ++mt) {
+      sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+      #pragma unroll
+      for (int ks = 0; ks < C::kKSteps; ++ks) {
+        if (!landed) break;
+        const int d0 = warp * C::kDPerWarp + ks * 16;
+        const int c = d0 >> 6;
+        const int u = ((d0 & 63) >> 3) + qk_unit_add;
+        const uint32_t addr = kbase + mt * C::kPageBytes + c * kChunkBytes + qk_row * 128 +
+                              ((u ^ (qk_row & 7)) << 4);
+        uint32_t a[4];
+        ldsm_x4(addr, a);
+        mma_bf16_16816(sacc[mt], a, qf[ks][0], qf[ks][1]);
+      }
+    }
+    float* sb = sbuf + (consumed & 1) * C::kSBufFloats;
+    {
+      float* mine = sb + warp * kQHeadsPerUnit * C::kTileKeys;
+      #pragma unroll
+      for (int mt = 0; mt < TP; ++mt) {
+        const int k0 = mt * 16 + g;
+        const int qa = 2 * t4, qb = 2 * t4 + 1;
+        mine[qa * C::kTileKeys + sbuf_key(qa, k0)] = sacc[mt][0];
+        mine[qb * C::kTileKeys + sbuf_key(qb, k0)] = sacc[mt][1];
+        mine[qa * C::kTileKeys + sbuf_key(qa, k0 + 8)] = sacc[mt][2];
+        mine[qb * C::kTileKeys + sbuf_key(qb, k0 + 8)] = sacc[mt][3];
+      }
+    }
+    named_bar_sync(1, kConsumerWarps * 32);
+    if (*cons_abort) {
+      if (lane == 0) *abort_flag = 1;  // stops the producer at its next tile
+      break;
+    }
+
+    // ---- full scores for qh = g, keys kk*16 + 2*t4 + {0, 1, 8, 9}
+    float sv[TP][4];
+    float mx = -INFINITY;
+    #pragma unroll
+    for (int kk = 0; kk < TP; ++kk) {
+      #pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kk * 16 + e * 8 + 2 * t4;
+        float2 acc = make_float2(0.f, 0.f);
+        #pragma unroll
+        for (int ww = 0; ww < kConsumerWarps; ++ww) {
+          const float2 v2 = *reinterpret_cast<const float2*>(
+              sb + (ww * kQHeadsPerUnit + g) * C::kTileKeys + sbuf_key(g, key));
+          acc.x += v2.x;
+          acc.y += v2.y;
+        }
+        float x0 = acc.x, x1 = acc.y;
+        if (use_cap) {
+          x0 = softcap * tanhf(x0 * scale / softcap) * kLog2e;
+          x1 = softcap * tanhf(x1 * scale / softcap) * kLog2e;
+        } else {
+          x0 *= scale_l2;
+          x1 *= scale_l2;
+        }
+        const int p0 = pos0 + key;
+        if (p0 < w.lo || p0 >= w.len) x0 = -INFINITY;
+        if (p0 + 1 < w.lo || p0 + 1 >= w.len) x1 = -INFINITY;
+        sv[kk][2 * e] = x0;
+        sv[kk][2 * e + 1] = x1;
+        mx = fmaxf(mx, fmaxf(x0, x1));
+      }
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);  // finite: every tile holds a visible key
+    const float alpha = exp2f(m_run - m_new);
+    // P = P_hi + P_lo, both bf16: the PV product then carries P to ~2^-17
+    // relative instead of bf16's 2^-9.
+    uint32_t pf[TP][2], pl[TP][2];
+    float psum = 0.f;
+    #pragma unroll
+    for (int kk = 0; kk < TP; ++kk) {
+      const float p0 = exp2f(sv[kk][0] - m_new), p1 = exp2f(sv[kk][1] - m_new);
+      const float p2 = exp2f(sv[kk][2] - m_new), p3 = exp2f(sv[kk][3] - m_new);
+      psum += (p0 + p1) + (p2 + p3);
+      pf[kk][0] = pack_bf16x2(p0, p1);
+      pf[kk][1] = pack_bf16x2(p2, p3);
+      const float2 h0 = unpack_bf16x2(pf[kk][0]), h1 = unpack_bf16x2(pf[kk][1]);
+      pl[kk][0] = pack_bf16x2(p0 - h0.x, p1 - h0.y);
+      pl[kk][1] = pack_bf16x2(p2 - h1.x, p3 - h1.y);
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+
+    // ---- zero the V rows of partially visible pages (this warp's chunks)
+    #pragma unroll
+    for (int kk = 0; kk < TP; ++kk) {
+      const int pf_pos = pos0 + kk * kBlockSize;
+      const int r_lo = max(0, w.lo - pf_pos);
+      const int r_hi = min(kBlockSize, w.len - pf_pos);
+      if (kk < npages && (r_lo > 0 || r_hi < kBlockSize)) {
+        uint8_t* vpage = stages + stage * C::kStageBytes + (KEQV ? 0 : C::kKTileBytes) +
+                         kk * C::kPageBytes;
+        for (int idx = lane; idx < kBlockSize * 8 * C::kChunksPerWarp; idx += 32) {
+          const int row = idx / (8 * C::kChunksPerWarp);
+          const int rem = idx - row * (8 * C::kChunksPerWarp);
+          const int c = warp * C::kChunksPerWarp + rem / 8;
+          const int u = rem & 7;
+          if (row < r_lo || row >= r_hi)
+            *reinterpret_cast<uint4*>(vpage + c * kChunkBytes + row * 128 + u * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+    }
+
+    // ---- rescale O^T and accumulate PV over this warp's quarter
+    const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t4) * 4);
+    const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t4 + 1) * 4);
+    #pragma unroll
+    for (int mt2 = 0; mt2 < C::kMTiles; ++mt2) {
+      o[mt2][0] *= a0;
+      o[mt2][1] *= a1;
+      o[mt2][2] *= a0;
+      o[mt2][3] *= a1;
+    }
+    #pragma unroll
+    for (int kk = 0; kk < TP; ++kk) {
+      if (kk < npages) {
+        #pragma unroll
+        for (int mt2 = 0; mt2 < C::kMTiles; ++mt2) {
+          const int d = warp * C::kDPerWarp + mt2 * 16 + pv_dadd;
+          const int c = d >> 6;
+          const int u = (d & 63) >> 3;
+          const uint32_t addr = vbase + kk * C::kPageBytes + c * kChunkBytes + pv_row * 128 +
+                                ((u ^ (pv_row & 7)) << 4);
+          uint32_t a[4];
+          ldsm_x4_trans(addr, a);
+          mma_bf16_16816(o[mt2], a, pf[kk][0], pf[kk][1]);
+          mma_bf16_16816(o[mt2], a, pl[kk][0], pl[kk][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[stage]);
+
+    // ---- end of this CTA's share of the unit: write the result or a partial
+    const bool unit_end = (w.tile == w.ntu - 1) || (t == t_end - 1);
+    if (unit_end) {
+      float l_tot = l_run;
+      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
+      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+      const int uf = w.unit_first_tile();
+      const bool complete = uf >= t_begin && uf + w.ntu - 1 < t_end;
+      const int64_t slot = static_cast<int64_t>(blockIdx.x) + w.global_unit();
+      #pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int qh = 2 * t4 + e;
+        const float lq = __shfl_sync(0xffffffffu, l_tot, qh * 4);
+        if (qh < nh) {
+          const float inv = 1.f / lq;
+          #pragma unroll
+          for (int mt2 = 0; mt2 < C::kMTiles; ++mt2) {
+            const int d = warp * C::kDPerWarp + mt2 * 16 + g;
+            if (complete) {
+              float* orow = out + (static_cast<int64_t>(w.s) * n_q + hb + qh) * HD;
+              orow[d] = o[mt2][e] * inv;
+              orow[d + 8] = o[mt2][2 + e] * inv;
+            } else {
+              float* prow = ws_o + (slot * kQHeadsPerUnit + qh) * HD;
+              prow[d] = o[mt2][e];
+              prow[d + 8] = o[mt2][2 + e];
+            }
+          }
+        }
+      }
+      if (warp == 0 && t4 == 0 && g < nh) {
+        if (complete) {
+          if (lse != nullptr)
+            lse[static_cast<int64_t>(w.s) * n_q + hb + g] = (m_run + log2f(l_tot)) * kLn2;
+        } else {
+          ws_ml[slot * kQHeadsPerUnit + g] = make_float2(m_run, l_tot);
+        }
+      }
+    }
+    w.advance();
+  }
+}
+
+// ---------------------------------------------------------------- merge
+// One CTA per unit. Units whose tiles sat in one CTA were written directly;
+// units with no visible key get zeros and lse = -inf; the rest combine
+// their partials: M = max m_i, l = sum l_i 2^(m_i - M),
+// out = sum O_i 2^(m_i - M) / l, lse = (M + log2 l) ln 2.
+template <int HD>
+__global__ void __launch_bounds__(256)
+decode_merge_kernel(const SeqPlan* __restrict__ plan, int n_seqs, int n_q, int n_kv, int group,
+                    int qchunks, int grid_main, float* __restrict__ out, float* __restrict__ lse,
+                    const float* __restrict__ ws_o, const float2* __restrict__ ws_ml) {
+  const int ups = n_kv * qchunks;
+  const int u = blockIdx.x;
+  const int s = u / ups, ul = u - s * ups;
+  const SeqPlan p = plan[s];
+  const int total = plan[n_seqs].tile_off;
+  const int kvh = ul / qchunks, qc = ul - kvh * qchunks;
+  const int hb = kvh * group + qc * kQHeadsPerUnit;
+  const int nh = min(kQHeadsPerUnit, group - qc * kQHeadsPerUnit);
+  if (p.ntu == 0) {
+    for (int i = threadIdx.x; i < nh * HD; i += blockDim.x)
+      out[(static_cast<int64_t>(s) * n_q + hb) * HD + i] = 0.f;
+    if (lse != nullptr && threadIdx.x < nh) lse[static_cast<int64_t>(s) * n_q + hb + threadIdx.x] = -INFINITY;
+    return;
+  }
+  const int per = (total + grid_main - 1) / grid_main;
+  const int t0 = p.tile_off + ul * p.ntu, t1 = t0 + p.ntu;
+  const int c0 = t0 / per, c1 = (t1 - 1) / per;
+  if (c0 == c1) return;
+  for (int qh = 0; qh < nh; ++qh) {
+    float M = -INFINITY;
+    for (int c = c0; c <= c1; ++c) M = fmaxf(M, ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh].x);
+    float Lsum = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      const float2 ml = ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh];
+      Lsum += ml.y * exp2f(ml.x - M);
+    }
+    const float inv = 1.f / Lsum;
+    for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+      float acc = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t slot = static_cast<int64_t>(c) + u;
+        const float wgt = exp2f(ws_ml[slot * kQHeadsPerUnit + qh].x - M);
+        acc += ws_o[(slot * kQHeadsPerUnit + qh) * HD + d] * wgt;
+      }
+      out[(static_cast<int64_t>(s) * n_q + hb + qh) * HD + d] = acc * inv;
+    }
+    if (threadIdx.x == 0 && lse != nullptr)
+      lse[static_cast<int64_t>(s) * n_q + hb + qh] = (M + log2f(Lsum)) * kLn2;
+  }
+}
+
+template <int HD, bool KEQV>
+int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CUtensorMap& v_map,
+           const int32_t* block_table, int max_blocks, int64_t num_blocks, const int32_t* seq_lens,
+           int n_seqs, float* out, float* lse, void* ws, size_t ws_bytes, int num_sms,
+           int32_t* err, cudaStream_t stream) {
+  using C = Cfg<HD, KEQV>;
+  const int grid = num_sms < kMaxDecodeCtas ? num_sms : kMaxDecodeCtas;
+  const DecodeWorkspace lay = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas);
+  if (ws_bytes < lay.total) return PSW_EWORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  SeqPlan* plan = reinterpret_cast<SeqPlan*>(base);
+  float* ws_o = reinterpret_cast<float*>(base + lay.o_offset);
+  float2* ws_ml = reinterpret_cast<float2*>(base + lay.ml_offset);
+
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(decode_split_kernel<HD, KEQV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return PSW_ELAUNCH;
+    attr_set[dev] = true;
+  }
+  const int ups = L.n_kv * L.qchunks();
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, n_seqs, L.window, max_blocks, ups,
+                                             C::kTilePages, plan, err);
+  decode_split_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
+      k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
+      plan, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.scale, L.softcap, out, lse, ws_o,
+      ws_ml, err);
+  decode_merge_kernel<HD><<<n_seqs * ups, 256, 0, stream>>>(
+      plan, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), grid, out, lse, ws_o, ws_ml);
+  return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
+}
+
+}  // namespace dec
+
+DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_ctas) {
+  DecodeWorkspace w{};
+  auto align = [](size_t x) { return (x + kDecodePlanAlign - 1) / kDecodePlanAlign * kDecodePlanAlign; };
+  const size_t slots = static_cast<size_t>(max_ctas) +
+                       static_cast<size_t>(n_seqs) * L.n_kv * L.qchunks();
+  w.plan_bytes = align((static_cast<size_t>(n_seqs) + 1) * sizeof(dec::SeqPlan));
+  w.o_bytes = align(slots * kQHeadsPerUnit * L.hd * sizeof(float));
+  w.ml_bytes = align(slots * kQHeadsPerUnit * sizeof(float2));
+  w.o_offset = w.plan_bytes;
+  w.ml_offset = w.o_offset + w.o_bytes;
+  w.total = w.ml_offset + w.ml_bytes;
+  return w;
+}
+
+int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
+                  const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
+                  int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse,
+                  void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream) {
+  if (n_seqs == 0) return PSW_OK;
+  if (L.hd == 256) {
+    return L.k_eq_v
+               ? dec::launch<256, true>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
+                                        seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
+                                        stream)
+               : dec::launch<256, false>(L, q, k_map, v_map, block_table, max_blocks,
+                                         num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
+                                         num_sms, err, stream);
+  }
+  return L.k_eq_v
+             ? dec::launch<512, true>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
+                                      seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
+                                      stream)
+             : dec::launch<512, false>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
+                                       seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
+                                       stream);
+}
+
+}  // namespace psw

@@ -1,0 +1,63 @@
+// psw_internal.h -- host-side launchers shared between the API translation
+// unit and the kernel translation units of libpsw. Library-internal.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/psw.h"
+
+namespace psw {
+
+constexpr int kBlockSize = 16;          // tokens per page
+constexpr int kMaxDecodeCtas = 512;     // upper bound on the persistent decode grid
+constexpr int kQHeadsPerUnit = 8;       // query heads handled together per KV head
+constexpr int kDecodePlanAlign = 256;
+
+struct LayerArgs {
+  int n_q, n_kv, hd, window;
+  float softcap, scale;
+  bool k_eq_v;
+  int group() const { return n_q / n_kv; }
+  int qchunks() const { return (group() + kQHeadsPerUnit - 1) / kQHeadsPerUnit; }
+};
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int cc_major, cc_minor;
+};
+
+// Current device's properties (cached per device).
+cudaError_t device_info(DeviceInfo* info);
+
+// Per-device error word used by every kernel (device pointer).
+int32_t* device_error_word();
+
+// Decode workspace layout (bytes): plan | partial O | partial (m, l).
+struct DecodeWorkspace {
+  size_t plan_bytes, o_bytes, ml_bytes, total;
+  size_t o_offset, ml_offset;
+};
+DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_ctas);
+
+cudaError_t launch_kv_cache_write(const LayerArgs& L, const void* k, const void* v,
+                                  const int32_t* cu_new, const int32_t* past_lens, int n_seqs,
+                                  const int32_t* block_table, int max_blocks, int64_t num_blocks,
+                                  void* k_pool, void* v_pool, int num_sms, int32_t* err,
+                                  cudaStream_t stream);
+
+// Returns a PSW_* code.
+int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
+                  const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
+                  int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse, void* ws,
+                  size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream);
+
+// Builds the TMA descriptor of a pool seen as [slot][chunk of 64 elems][64]
+// with one box = 16 slots x 1 chunk, 128-byte swizzle.
+int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
+                         int hd);
+
+}  // namespace psw

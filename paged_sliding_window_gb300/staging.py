@@ -1,0 +1,71 @@
+"""Stages a seeded workload step on the GPU for the C ABI: device copies of
+the step's inputs, canary-filled pools with the retained history written by
+the library's own kv_cache_write, output buffers and the workspace. Used by
+the benchmark and the GPU tests; all compute goes through ``binding``."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding
+from . import workloads as wl
+
+
+def dev_bf16(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def dev_i32(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class GpuStep:
+    """Device copies of one step's inputs plus pools with the history written."""
+
+    def __init__(self, step: wl.Step, device="cuda"):
+        self.step = step
+        layer = step.layer
+        c = step.cache
+        shape = c.pool_shape
+        canary = int(wl.CANARY_BF16)  # < 0x8000, so the same bits as int16
+        self.k_pool = torch.full(shape, canary, dtype=torch.int16, device=device).view(torch.bfloat16)
+        self.v_pool = None if layer.k_eq_v else torch.full(
+            shape, canary, dtype=torch.int16, device=device).view(torch.bfloat16)
+        self.table = dev_i32(step.block_table, device)
+        self.pages = binding.make_pages(self.table, c.num_blocks)
+        if c.hist_k.shape[0] > 0:
+            binding.kv_cache_write(layer, dev_bf16(c.hist_k, device),
+                                   None if layer.k_eq_v else dev_bf16(c.hist_v, device),
+                                   dev_i32(c.hist_cu, device), dev_i32(c.hist_past, device),
+                                   self.pages, self.k_pool, self.v_pool)
+        self.q = dev_bf16(step.q, device)
+        self.new_k = dev_bf16(step.new_k, device)
+        self.new_v = None if layer.k_eq_v else dev_bf16(step.new_v, device)
+        self.cu_new = dev_i32(step.cu_new, device)
+        self.past = dev_i32(step.past_lens, device)
+        self.seq_lens = dev_i32(step.seq_lens, device)
+        n_rows = step.q.shape[0]
+        self.out = torch.full((n_rows, layer.n_q_heads, layer.head_dim), float("nan"),
+                              dtype=torch.float32, device=device)
+        self.lse = torch.full((n_rows, layer.n_q_heads), float("nan"), dtype=torch.float32,
+                              device=device)
+        max_len = int(step.seq_lens.max()) if step.n_seqs else 0
+        self.ws = binding.alloc_workspace(layer, step.n_seqs, max_len, device)
+
+    def write_new(self):
+        binding.kv_cache_write(self.step.layer, self.new_k, self.new_v, self.cu_new, self.past,
+                               self.pages, self.k_pool, self.v_pool)
+
+    def decode(self):
+        binding.attn_decode_paged(self.step.layer, self.q, self.k_pool, self.v_pool, self.pages,
+                                  self.seq_lens, self.out, self.lse, self.ws)
+
+    def prefill(self):
+        max_q = int(self.step.new_lens.max()) if self.step.n_seqs else 0
+        binding.attn_prefill_chunked(self.step.layer, self.q, self.cu_new, self.past, max_q,
+                                     self.k_pool, self.v_pool, self.pages, self.out, self.lse,
+                                     self.ws)
