@@ -82,6 +82,8 @@ typedef struct CUstream_st *psw_stream_t;
 #define PSW_EDEVICE          -13  /* no usable sm_103 device */
 #define PSW_ELAUNCH          -14  /* a CUDA launch or attribute call failed */
 #define PSW_ETENSORMAP       -15  /* the TMA descriptor for a pool could not be built */
+#define PSW_ESCRATCH         -16  /* the batch needs more scratch than the static buffer of
+                                     attn_decode_paged_noalloc holds */
 
 /* ---- device error bits (psw_get_error) ---- */
 #define PSW_DEVERR_BLOCK_ID    1  /* block id outside [0, num_blocks): access skipped */
@@ -175,6 +177,35 @@ PSW_API int attn_prefill_chunked(const psw_layer_t *layer, const void *q, const 
                          const void *k_pool, const void *v_pool, const psw_pages_t *pages,
                          float *out, float *lse, void *ws, size_t ws_bytes,
                          psw_stream_t stream);
+
+/*
+ * attn_decode_paged for callers that cannot allocate device memory (their
+ * device memory belongs to another allocator with a fixed budget, or they must
+ * not call cudaMalloc once serving has started). The pages have no counterpart
+ * for this entry point; it is a property of this library only.
+ *
+ * Arguments, results and errors are those of attn_decode_paged, without the
+ * workspace: the scratch comes from a static device buffer of
+ * PSW_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
+ * library holds until the process exits. A batch whose workspace
+ * (psw_workspace_bytes) exceeds that size returns PSW_ESCRATCH before anything
+ * runs: with head_dim 256 that is more than about 1500 units, with head_dim
+ * 512 more than about 500, where units = n_seqs * n_kv_heads *
+ * ceil((n_q_heads / n_kv_heads) / 8).
+ *
+ * The first call on a device looks up the buffer's device address (with that
+ * device current) and keeps it; make that first call before any stream
+ * capture. Nothing is allocated or freed, ever. All calls share the buffer and
+ * it keeps the last call's contents; nothing in it needs to start at zero.
+ * Calls whose kernels could overlap on the GPU (several streams or host
+ * threads on one device) race on the buffer: serialise them.
+ */
+#define PSW_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+PSW_API int attn_decode_paged_noalloc(const psw_layer_t *layer, const void *q,
+                                      const void *k_pool, const void *v_pool,
+                                      const psw_pages_t *pages, const int32_t *seq_lens,
+                                      int32_t n_seqs, float *out, float *lse,
+                                      psw_stream_t stream);
 
 /*
  * Synchronises `stream`, then returns the current device's error word (an OR

@@ -22,11 +22,12 @@ ERRORS = {
     -5: "PSW_EINVAL_WINDOW", -6: "PSW_EINVAL_BLOCKSIZE", -7: "PSW_EINVAL_KEQV",
     -8: "PSW_EINVAL_SCALE", -9: "PSW_EINVAL_NSEQS", -10: "PSW_EWORKSPACE",
     -11: "PSW_ECAPACITY", -12: "PSW_EALIGN", -13: "PSW_EDEVICE", -14: "PSW_ELAUNCH",
-    -15: "PSW_ETENSORMAP",
+    -15: "PSW_ETENSORMAP", -16: "PSW_ESCRATCH",
 }
 DEVERR_BLOCK_ID, DEVERR_CAPACITY, DEVERR_LENGTH, DEVERR_PIPELINE = 1, 2, 4, 8
 EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
-            "attn_prefill_chunked", "psw_get_error", "psw_strerror")
+            "attn_prefill_chunked", "psw_get_error", "psw_strerror",
+            "attn_decode_paged_noalloc")
 
 
 class PswLayer(ctypes.Structure):
@@ -75,6 +76,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.attn_decode_paged.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz, vp]
         lib.attn_prefill_chunked.argtypes = [lp, vp, vp, vp, i32, i32, vp, vp, pp, vp, vp, vp,
                                              sz, vp]
+        lib.attn_decode_paged_noalloc.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp]
+        lib.attn_decode_paged_noalloc.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.psw_strerror.argtypes = [ctypes.c_int]
         lib.psw_strerror.restype = ctypes.c_char_p
@@ -186,6 +189,24 @@ def attn_prefill_chunked(layer, q, cu_q, past_lens, max_q_len: int, k_pool, v_po
                                      _ptr(k_pool), _ptr(v_pool), ctypes.byref(pages), _ptr(out),
                                      _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
     _raise(rc, "attn_prefill_chunked")
+
+
+def attn_decode_paged_noalloc(layer, q, k_pool, v_pool, pages: PswPages, seq_lens, out,
+                              lse=None, stream=None) -> None:
+    """attn_decode_paged without a workspace, for callers that cannot allocate
+    device memory: the library uses its own static device buffer (see
+    include/psw.h for the size limit and the rule that overlapping calls race)."""
+    _check(q, torch.bfloat16, "q")
+    _check(k_pool, torch.bfloat16, "k_pool")
+    _check(v_pool, torch.bfloat16, "v_pool")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(out, torch.float32, "out")
+    _check(lse, torch.float32, "lse")
+    rc = load().attn_decode_paged_noalloc(ctypes.byref(make_layer(layer)), _ptr(q),
+                                          _ptr(k_pool), _ptr(v_pool), ctypes.byref(pages),
+                                          _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(out),
+                                          _ptr(lse), _stream(stream))
+    _raise(rc, "attn_decode_paged_noalloc")
 
 
 def get_error(stream=None) -> int:

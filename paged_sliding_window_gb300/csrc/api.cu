@@ -282,6 +282,8 @@ const char* psw_strerror(int code) {
     case PSW_EDEVICE: return "no usable sm_103 (GB300) device";
     case PSW_ELAUNCH: return "CUDA launch failed";
     case PSW_ETENSORMAP: return "could not build the TMA descriptor of a pool";
+    case PSW_ESCRATCH:
+      return "batch needs more scratch than the static buffer of attn_decode_paged_noalloc";
     default: return "unknown error";
   }
 }
