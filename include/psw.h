@@ -164,16 +164,21 @@ PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const voi
  * past_lens[b] + i and attends over keys [0, past_lens[b] + i] under the band
  * and causal rules. The chunk's own K/V must already be in the pages
  * (kv_cache_write first).
- *   q          device bf16 [n_q_total][n_q_heads][head_dim], n_q_total = cu_q[n_seqs]
- *   cu_q       device int32 [n_seqs + 1]; past_lens device int32 [n_seqs]
+ *   q          device bf16 [n_q_total][n_q_heads][head_dim]
+ *   cu_q       device int32 [n_seqs + 1], non-decreasing, cu_q[n_seqs] <= n_q_total
+ *   past_lens  device int32 [n_seqs]
+ *   n_q_total  host: rows of q and out
+ *   max_q_len  host bound on every chunk length (cu_q[b+1] - cu_q[b]); longer
+ *              chunks are flagged (PSW_DEVERR_LENGTH) and their excess rows skipped
  *   out        device fp32 [n_q_total][n_q_heads][head_dim]; lse fp32 [n_q_total][n_q_heads] or NULL
- *   max_q_len  host bound on every chunk length (cu_q[b+1] - cu_q[b])
- *   ws         as for attn_decode_paged
- * Tensor-core kernel (tcgen05/TMEM with TMA-fed tiles); key tiles that the
- * band rule hides from every row of a query tile are never loaded.
+ *   ws, ws_bytes  unused by this kernel (may be NULL / 0)
+ * Tensor-core kernel (tcgen05 MMAs with S, P and O in tensor memory, K/V tiles
+ * fed by TMA through the block table); key tiles that the band rule hides from
+ * every row of a query tile are never loaded. Needs n_q_heads / n_kv_heads <= 128.
  */
 PSW_API int attn_prefill_chunked(const psw_layer_t *layer, const void *q, const int32_t *cu_q,
-                         const int32_t *past_lens, int32_t n_seqs, int32_t max_q_len,
+                         const int32_t *past_lens, int32_t n_seqs, int32_t n_q_total,
+                         int32_t max_q_len,
                          const void *k_pool, const void *v_pool, const psw_pages_t *pages,
                          float *out, float *lse, void *ws, size_t ws_bytes,
                          psw_stream_t stream);

@@ -74,8 +74,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.psw_workspace_bytes.argtypes = [lp, i32, i32, ctypes.POINTER(sz)]
         lib.kv_cache_write.argtypes = [lp, vp, vp, vp, vp, i32, pp, vp, vp, vp]
         lib.attn_decode_paged.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz, vp]
-        lib.attn_prefill_chunked.argtypes = [lp, vp, vp, vp, i32, i32, vp, vp, pp, vp, vp, vp,
-                                             sz, vp]
+        lib.attn_prefill_chunked.argtypes = [lp, vp, vp, vp, i32, i32, i32, vp, vp, pp, vp, vp,
+                                             vp, sz, vp]
         lib.attn_decode_paged_noalloc.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp]
         lib.attn_decode_paged_noalloc.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -185,7 +185,8 @@ def attn_prefill_chunked(layer, q, cu_q, past_lens, max_q_len: int, k_pool, v_po
     _check(lse, torch.float32, "lse")
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     rc = load().attn_prefill_chunked(ctypes.byref(make_layer(layer)), _ptr(q), _ptr(cu_q),
-                                     _ptr(past_lens), int(past_lens.shape[0]), int(max_q_len),
+                                     _ptr(past_lens), int(past_lens.shape[0]), int(q.shape[0]),
+                                     int(max_q_len),
                                      _ptr(k_pool), _ptr(v_pool), ctypes.byref(pages), _ptr(out),
                                      _ptr(lse), _ptr(ws), ws_bytes, _stream(stream))
     _raise(rc, "attn_prefill_chunked")

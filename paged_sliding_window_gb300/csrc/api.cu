@@ -148,6 +148,24 @@ int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks,
   return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
 }
 
+int make_query_tensor_map(CUtensorMap* map, const void* q, int n_q_total, int n_q, int hd,
+                          int group) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return PSW_ETENSORMAP;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(n_q),
+                              static_cast<cuuint64_t>(n_q_total)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2,
+                                 static_cast<cuuint64_t>(n_q) * hd * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(128 / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
+}
+
 }  // namespace psw
 
 using namespace psw;
@@ -223,10 +241,10 @@ int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_poo
 }
 
 int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t* cu_q,
-                         const int32_t* past_lens, int32_t n_seqs, int32_t max_q_len,
-                         const void* k_pool, const void* v_pool, const psw_pages_t* pages,
-                         float* out, float* lse, void* ws, size_t ws_bytes,
-                         psw_stream_t stream) {
+                         const int32_t* past_lens, int32_t n_seqs, int32_t n_q_total,
+                         int32_t max_q_len, const void* k_pool, const void* v_pool,
+                         const psw_pages_t* pages, float* out, float* lse, void* ws,
+                         size_t ws_bytes, psw_stream_t stream) {
   LayerArgs L;
   int rc = check_layer(layer, &L);
   if (rc != PSW_OK) return rc;
@@ -236,16 +254,29 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
   if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
   if ((rc = check_pages(pages)) != PSW_OK) return rc;
   if (n_seqs < 0) return PSW_EINVAL_NSEQS;
-  if (max_q_len < 0) return PSW_ECAPACITY;
+  if (L.group() > 128) return PSW_EINVAL_HEADS;
+  if (max_q_len < 0 || n_q_total < 0) return PSW_ECAPACITY;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PSW_EALIGN;
   (void)ws;
   (void)ws_bytes;
-  (void)stream;
-  (void)lse;
-  if (n_seqs == 0 || max_q_len == 0) return PSW_OK;
+  if (n_seqs == 0 || max_q_len == 0 || n_q_total == 0) return PSW_OK;
+  if (n_seqs > 65535) return PSW_EINVAL_NSEQS;
   DeviceState* st;
   if ((rc = device_ready(&st)) != PSW_OK) return rc;
-  return PSW_ELAUNCH;  // prefill kernel not built yet
+  CUtensorMap q_map, k_map, v_map;
+  if ((rc = make_query_tensor_map(&q_map, q, n_q_total, L.n_q, L.hd, L.group())) != PSW_OK)
+    return rc;
+  if ((rc = make_pool_tensor_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd)) != PSW_OK)
+    return rc;
+  if (L.k_eq_v) {
+    v_map = k_map;
+  } else if ((rc = make_pool_tensor_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd)) !=
+             PSW_OK) {
+    return rc;
+  }
+  return launch_prefill(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs, n_q_total, max_q_len,
+                        pages->block_table, pages->max_blocks_per_seq, pages->num_blocks, out,
+                        lse, st->err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int psw_get_error(psw_stream_t stream, int32_t* device_error_out) {

@@ -98,7 +98,7 @@ def _write(lib, layer, k=FAKE, v=FAKE, cu=FAKE, past=FAKE, n=4, pages=None, kp=F
 def _prefill(lib, layer, q=FAKE, cu=FAKE, past=FAKE, n=4, maxq=512, k=FAKE, v=FAKE, pages=None,
              out=FAKE):
     pages = pages or _pages()
-    return lib.attn_prefill_chunked(ctypes.byref(layer), q, cu, past, n, maxq, k, v,
+    return lib.attn_prefill_chunked(ctypes.byref(layer), q, cu, past, n, 4 * 512, maxq, k, v,
                                     ctypes.byref(pages), out, None, FAKE, 1 << 30, None)
 
 

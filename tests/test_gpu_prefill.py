@@ -1,0 +1,124 @@
+"""Chunked-prefill parity on the GPU: kv_cache_write of the chunk then
+attn_prefill_chunked through the C ABI, against the fp64 oracle. Pools are
+compared bit for bit; outputs within 2e-3 + 1e-2 |ref|."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import GpuStep, OracleStep, assert_close, host_bits
+from paged_sliding_window_gb300 import binding
+from paged_sliding_window_gb300 import workloads as wl
+from paged_sliding_window_gb300.workloads import Layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    return oracle.default()
+
+
+def sample_rows(step, every=7, edge=64):
+    """First and last `edge` rows of each chunk, every `every`-th row, and the
+    rows around the window boundary of each chunk."""
+    rows = set()
+    W = step.layer.window
+    for b in range(step.n_seqs):
+        lo, hi = int(step.cu_new[b]), int(step.cu_new[b + 1])
+        n = hi - lo
+        rows.update(range(lo, min(hi, lo + edge)))
+        rows.update(range(max(lo, hi - edge), hi))
+        rows.update(range(lo, hi, every))
+        if W > 0:
+            past = int(step.past_lens[b])
+            for i in (W - past - 2, W - past - 1, W - past, W - past + 1):
+                if 0 <= i < n:
+                    rows.add(lo + i)
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def run_prefill(orc, step, rows=None, check_pools=True):
+    g = GpuStep(step)
+    g.write_new()
+    g.prefill()
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    o = OracleStep(orc, step)
+    if check_pools:
+        assert np.array_equal(host_bits(g.k_pool), o.k_pool), "K pool differs from the oracle"
+        if g.v_pool is not None:
+            assert np.array_equal(host_bits(g.v_pool), o.v_pool), "V pool differs from the oracle"
+    ref_out, ref_lse = o.prefill(rows)
+    got_out = g.out.cpu().numpy()
+    got_lse = g.lse.cpu().numpy()
+    if rows is not None:
+        got_out, got_lse = got_out[rows], got_lse[rows]
+    assert_close(got_out, ref_out, "prefill out")
+    assert_close(got_lse, ref_lse, "prefill lse")
+    return g
+
+
+def test_chunked_prefill_softcap_full_size_sampled(orc):
+    step = wl.chunked_prefill().steps[0]
+    g = run_prefill(orc, step, rows=sample_rows(step))
+    assert torch.isfinite(g.out).all() and torch.isfinite(g.lse).all()
+
+
+PREFILL_CASES = [
+    # layer, past lens, chunk lens
+    pytest.param(Layer(8, 4, 256, window=64, softcap=50.0, scale=0.0625),
+                 [0, 10, 63, 64, 65, 200, 1000], [1, 70, 64, 63, 129, 5, 300], id="hd256-g2-w64-cap"),
+    pytest.param(Layer(16, 8, 256, window=1024), [0, 3000, 1020, 17], [700, 65, 9, 1024],
+                 id="hd256-g2-w1024"),
+    pytest.param(Layer(8, 8, 256, window=0), [0, 5, 130], [130, 33, 64], id="hd256-g1-full"),
+    pytest.param(Layer(16, 2, 256, window=40, softcap=20.0), [0, 77, 500], [50, 33, 17],
+                 id="hd256-g8-w40-cap"),
+    pytest.param(Layer(32, 2, 256, window=0, scale=0.3), [0, 12], [40, 9], id="hd256-g16-full"),
+    pytest.param(Layer(32, 4, 512, window=0, k_eq_v=True), [0, 100, 1500], [48, 17, 200],
+                 id="hd512-g8-keqv"),
+    pytest.param(Layer(8, 2, 512, window=48), [0, 30, 400], [100, 3, 60], id="hd512-g4-w48"),
+    pytest.param(Layer(4, 4, 256, window=0, k_eq_v=True), [0, 31], [31, 66], id="hd256-g1-keqv"),
+    pytest.param(Layer(12, 4, 256, window=33), [0, 50], [45, 20], id="hd256-g3-w33"),
+]
+
+
+@pytest.mark.parametrize("layer,past,chunks", PREFILL_CASES)
+def test_prefill_edge_cases(orc, layer, past, chunks):
+    step = wl.custom_step(layer, 31, past, chunks)
+    run_prefill(orc, step)
+
+
+def test_prefill_last_row_matches_decode():
+    """Row i of a chunk and a decode at seq_len = past + i + 1 see the same keys
+    (the decode tail rule equals the band rule); the two kernels agree."""
+    layer = Layer(16, 8, 256, window=256, softcap=30.0)
+    past, chunk = np.array([700, 40, 300]), np.array([64, 100, 1])
+    step = wl.custom_step(layer, 41, past, chunk)
+    g = GpuStep(step)
+    g.write_new()
+    g.prefill()
+    last = step.cu_new[1:] - 1
+    q_last = g.q[torch.from_numpy(last.astype(np.int64)).cuda()].contiguous()
+    out = torch.empty((3, 16, 256), dtype=torch.float32, device="cuda")
+    lse = torch.empty((3, 16), dtype=torch.float32, device="cuda")
+    seq_lens = torch.from_numpy((past + chunk).astype(np.int32)).cuda()
+    binding.attn_decode_paged(layer, q_last, g.k_pool, g.v_pool, g.pages, seq_lens, out, lse,
+                              g.ws)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert_close(out.cpu().numpy(), g.out[torch.from_numpy(last.astype(np.int64)).cuda()].cpu().numpy(),
+                 "decode vs prefill last row")
+
+
+def test_prefill_invalid_block_is_flagged():
+    layer = Layer(8, 4, 256, window=64)
+    step = wl.custom_step(layer, 51, [100, 20], [40, 40])
+    g = GpuStep(step)
+    g.write_new()
+    assert binding.get_error() == 0
+    bad = g.table.clone()
+    bad[0, 7] = step.cache.num_blocks + 1
+    g.pages = binding.make_pages(bad, step.cache.num_blocks)
+    g.prefill()
+    assert binding.get_error() & binding.DEVERR_BLOCK_ID
