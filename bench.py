@@ -72,6 +72,20 @@ def io_bytes(step: wl.Step) -> int:
     return n * L.n_q_heads * (L.head_dim * 2 + L.head_dim * 4 + 4)
 
 
+def prefill_flops(step: wl.Step) -> int:
+    """Algorithmic FLOPs of one prefill launch: 4 * head_dim per visible
+    (row, key) pair per query head (2 for q.k, 2 for p.v); masked and skipped
+    work is not counted."""
+    L = step.layer
+    total = 0
+    for b in range(step.n_seqs):
+        n = int(step.new_lens[b])
+        pos = int(step.past_lens[b]) + np.arange(n, dtype=np.int64)
+        vis = np.minimum(pos + 1, L.window) if L.window > 0 else pos + 1
+        total += int(vis.sum())
+    return 4 * L.head_dim * L.n_q_heads * total
+
+
 def source_sha() -> str:
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
@@ -225,6 +239,108 @@ def config_of(step: wl.Step) -> dict:
             "parallelism": "replicas"}
 
 
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_calls(fn, n, warmup, flush=None):
+    """Mean CUDA-event time (ms) of fn() on the current stream, L2 flushed
+    before each timed call when `flush` is given."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    times = []
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in times)
+
+
+def measure_prefill(steps, warmup, tflops_peak, peak_kind):
+    """Chunked prefill with softcap: kv_cache_write of the chunks, then
+    attn_prefill_chunked; TFLOP/s of the prefill call."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+    from paged_sliding_window_gb300.staging import GpuStep
+    step = wl.chunked_prefill().steps[0]
+    g = GpuStep(step)
+    flops = prefill_flops(step)
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    write_ms = time_calls(g.write_new, steps, warmup, lambda: flush_l2(scratch))
+    call_ms = time_calls(g.prefill, steps, warmup, lambda: flush_l2(scratch))
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    achieved = flops / (call_ms / 1e3) / 1e12
+    return {"workload": "chunked prefill with softcap", "metric": "prefill attn TFLOP/s",
+            "value": achieved, "unit": "TFLOP/s", "ms_per_call": call_ms,
+            "kv_cache_write_ms": write_ms, "flops_per_call": flops,
+            "config": {"n_seqs": 8, "past": "uniform [0, 8192]", "chunk": 512, "head_dim": 256,
+                       "n_q_heads": 8, "n_kv_heads": 4, "window": 1024, "softcap": 50.0,
+                       "scale": 1 / 16, "l2": "flushed (256 MB write) before every timed call"},
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel<256, false>",
+                         "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tflops_peak, "peak_kind": peak_kind + " bf16 burst",
+                         "traffic": None},
+            "gpu_launches_per_call": 1}
+
+
+def measure_full_decode(steps, warmup, hbm, peak_kind):
+    """Full-layer k_eq_v decode: KV-read GB/s of attn_decode_paged."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+    from paged_sliding_window_gb300.staging import GpuStep
+    step = wl.full_keqv_decode().steps[0]
+    g = GpuStep(step)
+    g.write_new()
+    nbytes = kv_bytes(step)
+    call_ms = time_calls(g.decode, steps, warmup)
+    assert binding.get_error() == 0
+    gbs = nbytes / (call_ms / 1e3) / 1e9
+    achieved = (nbytes + io_bytes(step)) / (call_ms / 1e3) / 1e9
+    return {"workload": "full-layer k_eq_v decode", "metric": "decode attn KV-read GB/s",
+            "value": gbs, "unit": "GB/s", "ms_per_call": call_ms, "kv_bytes_per_call": nbytes,
+            "config": {"n_seqs": 32, "seq_len": "log-uniform [1024, 32768]", "head_dim": 512,
+                       "n_q_heads": 32, "n_kv_heads": 4, "k_eq_v": True,
+                       "l2": "inputs larger than L2, no flush"},
+            "roofline": {"bound": "hbm", "kernel": "attn_decode_paged (plan + split + merge)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None}}
+
+
+def ncu_case(which):
+    """A reduced-memory copy of one bench launch for `ncu --set full`: the same
+    per-launch work with the pool sized to what the batch needs."""
+    import torch
+    from paged_sliding_window_gb300 import build
+    from paged_sliding_window_gb300.staging import GpuStep
+    build.build()
+    if which == "decode":
+        full = wl.sliding_decode().steps[0]
+        ss = np.random.SeedSequence(2)
+        rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
+        lens = wl.uniform_int(rng, 512, 4096, 64)
+        step = wl.custom_step(full.layer, 2, lens - 1, np.ones(64, np.int64), threads=8)
+        g = GpuStep(step)
+        g.write_new()
+        for _ in range(3):
+            g.decode()
+    else:
+        step = wl.chunked_prefill().steps[0]
+        g = GpuStep(step)
+        g.write_new()
+        for _ in range(3):
+            g.prefill()
+    torch.cuda.synchronize()
+    print(f"ncu case {which} done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -232,7 +348,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the prefill and full-layer decode measurements")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None)
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -355,6 +477,10 @@ def main():
         "stage_ms": {"kv_cache_write": write_ms, "attn_decode_paged": decode_ms},
         "clocks": clock_info,
     }
+    if not args.no_extra:
+        hbm_p, tf_p, kind_p = peaks()
+        line["prefill"] = measure_prefill(args.steps, args.warmup, tf_p, kind_p)
+        line["full_keqv_decode"] = measure_full_decode(args.steps, args.warmup, hbm_p, kind_p)
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
