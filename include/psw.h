@@ -31,7 +31,8 @@
  * Conventions for every call:
  *  - Pointers named as device pointers must be device memory of the current
  *    device (or managed memory); the library never copies host buffers.
- *    Every bf16 tensor pointer (q, k, v, pools) must be 16-byte aligned.
+ *    Every bf16 tensor pointer (q, k, v, pools) and every `out` must be
+ *    16-byte aligned.
  *  - The caller owns every buffer: inputs, pools, tables, outputs and the
  *    workspace. The library allocates and frees nothing.
  *  - Calls are asynchronous on `stream` (NULL = legacy default stream) and do
@@ -78,7 +79,7 @@ typedef struct CUstream_st *psw_stream_t;
 #define PSW_EWORKSPACE       -10  /* workspace smaller than psw_workspace_bytes() */
 #define PSW_ECAPACITY        -11  /* max_blocks_per_seq or num_blocks <= 0, or
                                      max_seq_len > max_blocks_per_seq * 16 */
-#define PSW_EALIGN           -12  /* a bf16 tensor pointer is not 16-byte aligned */
+#define PSW_EALIGN           -12  /* a tensor pointer (bf16 inputs, pools, out) is not 16-byte aligned */
 #define PSW_EDEVICE          -13  /* no usable sm_103 device */
 #define PSW_ELAUNCH          -14  /* a CUDA launch or attribute call failed */
 #define PSW_ETENSORMAP       -15  /* the TMA descriptor for a pool could not be built */

@@ -220,7 +220,8 @@ int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_poo
   if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
   if ((rc = check_pages(pages)) != PSW_OK) return rc;
   if (n_seqs < 0) return PSW_EINVAL_NSEQS;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PSW_EALIGN;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PSW_EALIGN;
   if (n_seqs == 0) return PSW_OK;
   if (ws == nullptr) return PSW_EWORKSPACE;
   if (ws_bytes < decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total) return PSW_EWORKSPACE;
@@ -256,7 +257,8 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
   if (n_seqs < 0) return PSW_EINVAL_NSEQS;
   if (L.group() > 128) return PSW_EINVAL_HEADS;
   if (max_q_len < 0 || n_q_total < 0) return PSW_ECAPACITY;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool)) return PSW_EALIGN;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PSW_EALIGN;
   (void)ws;
   (void)ws_bytes;
   if (n_seqs == 0 || max_q_len == 0 || n_q_total == 0) return PSW_OK;
@@ -309,7 +311,7 @@ const char* psw_strerror(int code) {
     case PSW_EINVAL_NSEQS: return "n_seqs must be >= 0";
     case PSW_EWORKSPACE: return "workspace is missing or smaller than psw_workspace_bytes()";
     case PSW_ECAPACITY: return "page table capacity out of range";
-    case PSW_EALIGN: return "bf16 tensors must be 16-byte aligned";
+    case PSW_EALIGN: return "bf16 inputs, pools and out must be 16-byte aligned";
     case PSW_EDEVICE: return "no usable sm_103 (GB300) device";
     case PSW_ELAUNCH: return "CUDA launch failed";
     case PSW_ETENSORMAP: return "could not build the TMA descriptor of a pool";

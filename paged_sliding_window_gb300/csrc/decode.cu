@@ -72,7 +72,7 @@ struct Cfg {
   static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kTileKeys;
   static constexpr int kTmaPerTile = kTilePages * kChunks * (KEQV ? 1 : 2);
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + 32;
+      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + 64;
   static_assert(kTmaPerTile <= 32, "one TMA box per producer lane");
   static_assert(kStages >= 2, "need a pipeline");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -87,13 +87,17 @@ __device__ __forceinline__ int sbuf_key(int qh, int key) {
 // ---------------------------------------------------------------- plan
 // One CTA: validates seq_lens, computes per-sequence tile counts and their
 // exclusive prefix. plan[n_seqs].tile_off holds the total.
+// It also zeroes the merge tickets of every unit and writes the output of
+// empty sequences (zeros, lse = -inf), which have no tiles.
 __global__ void __launch_bounds__(1024)
 decode_plan_kernel(const int32_t* __restrict__ seq_lens, int n_seqs, int window,
                    int max_blocks, int units_per_seq, int tile_pages,
-                   SeqPlan* __restrict__ plan, int32_t* err) {
+                   SeqPlan* __restrict__ plan, int32_t* __restrict__ tickets, int row_floats,
+                   int n_q, float* __restrict__ out, float* __restrict__ lse, int32_t* err) {
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < n_seqs * units_per_seq; i += blockDim.x) tickets[i] = 0;
   if (tid == 0) carry = 0;
   __syncthreads();
   const int cap = max_blocks * kBlockSize;
@@ -132,6 +136,12 @@ decode_plan_kernel(const int32_t* __restrict__ seq_lens, int n_seqs, int window,
     __syncthreads();
     const int excl = incl - tiles + (warp > 0 ? warp_tot[warp - 1] : 0);
     if (s < n_seqs) plan[s] = SeqPlan{carry + excl, len, lo, ntu};
+    if (s < n_seqs && ntu == 0) {  // no visible key: zero output, lse = -inf
+      float4* row = reinterpret_cast<float4*>(out + static_cast<int64_t>(s) * row_floats);
+      for (int i = 0; i < row_floats / 4; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lse != nullptr)
+        for (int i = 0; i < n_q; ++i) lse[static_cast<int64_t>(s) * n_q + i] = -INFINITY;
+    }
     __syncthreads();
     if (tid == 0) carry += warp_tot[(blockDim.x >> 5) - 1];
     __syncthreads();
@@ -178,6 +188,36 @@ struct Walker {
   __device__ int global_unit() const { return s * ups + unit; }
 };
 
+// ---------------------------------------------------------------- merge
+// Combines the partial results of unit u held by CTAs c0..c1 (slots c + u):
+// M = max m_i, l = sum l_i 2^(m_i - M), out = sum O_i 2^(m_i - M) / l,
+// lse = (M + log2 l) ln 2. Partials are read through L2 (written by other SMs).
+template <int HD>
+__device__ void merge_unit(int u, int c0, int c1, int nh, float* out_rows, float* lse_rows,
+                           const float* ws_o, const float2* ws_ml, int tid, int nthreads) {
+  for (int qh = 0; qh < nh; ++qh) {
+    float M = -INFINITY;
+    for (int c = c0; c <= c1; ++c)
+      M = fmaxf(M, __ldcg(&ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh].x));
+    float Lsum = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      const float2 ml = __ldcg(&ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh]);
+      Lsum += ml.y * exp2f(ml.x - M);
+    }
+    const float inv = 1.f / Lsum;
+    for (int d = tid; d < HD; d += nthreads) {
+      float acc = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t slot = static_cast<int64_t>(c) + u;
+        const float wgt = exp2f(__ldcg(&ws_ml[slot * kQHeadsPerUnit + qh].x) - M);
+        acc += __ldcg(&ws_o[(slot * kQHeadsPerUnit + qh) * HD + d]) * wgt;
+      }
+      out_rows[qh * HD + d] = acc * inv;
+    }
+    if (tid == 0 && lse_rows != nullptr) lse_rows[qh] = (M + log2f(Lsum)) * kLn2;
+  }
+}
+
 // ---------------------------------------------------------------- split
 template <int HD, bool KEQV>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -187,7 +227,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     int max_blocks, int64_t num_blocks, const SeqPlan* __restrict__ plan,
                     int n_seqs, int n_q, int n_kv, int group, int qchunks, float scale,
                     float softcap, float* __restrict__ out, float* __restrict__ lse,
-                    float* __restrict__ ws_o, float2* __restrict__ ws_ml, int32_t* err) {
+                    float* __restrict__ ws_o, float2* __restrict__ ws_ml,
+                    int32_t* __restrict__ tickets, int32_t* err) {
   using C = Cfg<HD, KEQV>;
   constexpr int TP = C::kTilePages;
   extern __shared__ uint8_t smem_raw[];
@@ -199,13 +240,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   uint64_t* empty_bar = full_bar + C::kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + C::kStages);
   volatile int* cons_abort = abort_flag + 1;  // written only by consumer warps
-
-  const int ups = n_kv * qchunks;
-  const int total = plan[n_seqs].tile_off;
-  const int per = (total + gridDim.x - 1) / gridDim.x;
-  const int t_begin = blockIdx.x * per;
-  const int t_end = min(total, t_begin + per);
-  if (t_begin >= t_end) return;
+  volatile int* merge_flag = abort_flag + 2;  // this CTA merges the current unit
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -215,16 +250,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     *abort_flag = 0;
     *cons_abort = 0;
+    *merge_flag = 0;
     fence_mbar_init();
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&k_map);
+    if (!KEQV) prefetch_tensormap(&v_map);
   }
   __syncthreads();
 
+  const int ups = n_kv * qchunks;
+  const int total = plan[n_seqs].tile_off;
+  const int per = (total + gridDim.x - 1) / gridDim.x;
+  const int t_begin = blockIdx.x * per;
+  const int t_end = min(total, t_begin + per);
+  if (t_begin >= t_end) return;
+
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&k_map);
-      if (!KEQV) prefetch_tensormap(&v_map);
-    }
     const uint64_t policy = l2_policy_evict_first();
     Walker w;
     w.init(plan, n_seqs, ups, t_begin);
@@ -281,9 +324,28 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   const float scale_l2 = scale * kLog2e;
   const bool use_cap = softcap > 0.f;
   float o[C::kMTiles][4];
-  uint32_t qf[C::kKSteps][2];
+  uint32_t qf[C::kKSteps][2], qn[C::kKSteps][2];
   float m_run = -INFINITY, l_run = 0.f;
   int nh = 0, hb = 0;
+  bool have_next = false;
+  // Q fragments (B operand of QK) of unit `unit` of sequence `sq` for this lane
+  auto load_q = [&](int sq, int unit, uint32_t (&dst)[C::kKSteps][2]) {
+    const int kvh = unit / qchunks, qc = unit - kvh * qchunks;
+    const int hb_u = kvh * group + qc * kQHeadsPerUnit;
+    const int nh_u = min(kQHeadsPerUnit, group - qc * kQHeadsPerUnit);
+    const __nv_bfloat16* qrow =
+        q + (static_cast<int64_t>(sq) * n_q + hb_u + g) * HD + warp * C::kDPerWarp + t4 * 2;
+    #pragma unroll
+    for (int ks = 0; ks < C::kKSteps; ++ks) {
+      if (g < nh_u) {
+        dst[ks][0] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16));
+        dst[ks][1] = __ldg(reinterpret_cast<const unsigned int*>(qrow + ks * 16 + 8));
+      } else {
+        dst[ks][0] = 0u;
+        dst[ks][1] = 0u;
+      }
+    }
+  };
 
   // per-lane ldmatrix geometry
   const int j8 = lane >> 3, r8 = lane & 7;
@@ -304,18 +366,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       const int kvh = w.unit / qchunks, qc = w.unit - (w.unit / qchunks) * qchunks;
       hb = kvh * group + qc * kQHeadsPerUnit;
       nh = min(kQHeadsPerUnit, group - qc * kQHeadsPerUnit);
-      const __nv_bfloat16* qrow =
-          q + (static_cast<int64_t>(w.s) * n_q + hb + g) * HD + warp * C::kDPerWarp + t4 * 2;
-      #pragma unroll
-      for (int ks = 0; ks < C::kKSteps; ++ks) {
-        if (g < nh) {
-          qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16);
-          qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8);
-        } else {
-          qf[ks][0] = 0u;
-          qf[ks][1] = 0u;
-        }
+      if (have_next) {
+        #pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) { qf[ks][0] = qn[ks][0]; qf[ks][1] = qn[ks][1]; }
+      } else {
+        load_q(w.s, w.unit, qf);
       }
+      // prefetch the next unit's Q (if this CTA reaches it) while this one runs
+      Walker nx = w;
+      nx.tile = nx.ntu - 1;
+      nx.advance();
+      have_next = nx.s < n_seqs && nx.unit_first_tile() < t_end;
+      if (have_next) load_q(nx.s, nx.unit, qn);
       #pragma unroll
       for (int i = 0; i < C::kMTiles; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       m_run = -INFINITY;
@@ -517,59 +579,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
           ws_ml[slot * kQHeadsPerUnit + g] = make_float2(m_run, l_tot);
         }
       }
+      if (!complete) {
+        // The CTA that finishes a unit's last segment merges all segments:
+        // each CTA publishes its partial, then takes a ticket; nobody waits.
+        const int u = w.global_unit();
+        const int c0 = uf / per, c1 = (uf + w.ntu - 1) / per;
+        __threadfence();
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (threadIdx.x == 0) *merge_flag = (atomicAdd(&tickets[u], 1) == c1 - c0);
+        named_bar_sync(1, kConsumerWarps * 32);
+        if (*merge_flag) {
+          __threadfence();
+          merge_unit<HD>(u, c0, c1, nh, out + (static_cast<int64_t>(w.s) * n_q + hb) * HD,
+                         lse == nullptr ? nullptr : lse + static_cast<int64_t>(w.s) * n_q + hb,
+                         ws_o, ws_ml, threadIdx.x, kConsumerWarps * 32);
+        }
+      }
     }
     w.advance();
-  }
-}
-
-// ---------------------------------------------------------------- merge
-// One CTA per unit. Units whose tiles sat in one CTA were written directly;
-// units with no visible key get zeros and lse = -inf; the rest combine
-// their partials: M = max m_i, l = sum l_i 2^(m_i - M),
-// out = sum O_i 2^(m_i - M) / l, lse = (M + log2 l) ln 2.
-template <int HD>
-__global__ void __launch_bounds__(256)
-decode_merge_kernel(const SeqPlan* __restrict__ plan, int n_seqs, int n_q, int n_kv, int group,
-                    int qchunks, int grid_main, float* __restrict__ out, float* __restrict__ lse,
-                    const float* __restrict__ ws_o, const float2* __restrict__ ws_ml) {
-  const int ups = n_kv * qchunks;
-  const int u = blockIdx.x;
-  const int s = u / ups, ul = u - s * ups;
-  const SeqPlan p = plan[s];
-  const int total = plan[n_seqs].tile_off;
-  const int kvh = ul / qchunks, qc = ul - kvh * qchunks;
-  const int hb = kvh * group + qc * kQHeadsPerUnit;
-  const int nh = min(kQHeadsPerUnit, group - qc * kQHeadsPerUnit);
-  if (p.ntu == 0) {
-    for (int i = threadIdx.x; i < nh * HD; i += blockDim.x)
-      out[(static_cast<int64_t>(s) * n_q + hb) * HD + i] = 0.f;
-    if (lse != nullptr && threadIdx.x < nh) lse[static_cast<int64_t>(s) * n_q + hb + threadIdx.x] = -INFINITY;
-    return;
-  }
-  const int per = (total + grid_main - 1) / grid_main;
-  const int t0 = p.tile_off + ul * p.ntu, t1 = t0 + p.ntu;
-  const int c0 = t0 / per, c1 = (t1 - 1) / per;
-  if (c0 == c1) return;
-  for (int qh = 0; qh < nh; ++qh) {
-    float M = -INFINITY;
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh].x);
-    float Lsum = 0.f;
-    for (int c = c0; c <= c1; ++c) {
-      const float2 ml = ws_ml[(static_cast<int64_t>(c) + u) * kQHeadsPerUnit + qh];
-      Lsum += ml.y * exp2f(ml.x - M);
-    }
-    const float inv = 1.f / Lsum;
-    for (int d = threadIdx.x; d < HD; d += blockDim.x) {
-      float acc = 0.f;
-      for (int c = c0; c <= c1; ++c) {
-        const int64_t slot = static_cast<int64_t>(c) + u;
-        const float wgt = exp2f(ws_ml[slot * kQHeadsPerUnit + qh].x - M);
-        acc += ws_o[(slot * kQHeadsPerUnit + qh) * HD + d] * wgt;
-      }
-      out[(static_cast<int64_t>(s) * n_q + hb + qh) * HD + d] = acc * inv;
-    }
-    if (threadIdx.x == 0 && lse != nullptr)
-      lse[static_cast<int64_t>(s) * n_q + hb + qh] = (M + log2f(Lsum)) * kLn2;
   }
 }
 
@@ -586,6 +613,7 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   SeqPlan* plan = reinterpret_cast<SeqPlan*>(base);
   float* ws_o = reinterpret_cast<float*>(base + lay.o_offset);
   float2* ws_ml = reinterpret_cast<float2*>(base + lay.ml_offset);
+  int32_t* tickets = reinterpret_cast<int32_t*>(base + lay.ticket_offset);
 
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -599,13 +627,12 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   }
   const int ups = L.n_kv * L.qchunks();
   decode_plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, n_seqs, L.window, max_blocks, ups,
-                                             C::kTilePages, plan, err);
+                                             C::kTilePages, plan, tickets, L.n_q * HD, L.n_q,
+                                             out, lse, err);
   decode_split_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
       k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
       plan, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.scale, L.softcap, out, lse, ws_o,
-      ws_ml, err);
-  decode_merge_kernel<HD><<<n_seqs * ups, 256, 0, stream>>>(
-      plan, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), grid, out, lse, ws_o, ws_ml);
+      ws_ml, tickets, err);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 
@@ -619,9 +646,11 @@ DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_
   w.plan_bytes = align((static_cast<size_t>(n_seqs) + 1) * sizeof(dec::SeqPlan));
   w.o_bytes = align(slots * kQHeadsPerUnit * L.hd * sizeof(float));
   w.ml_bytes = align(slots * kQHeadsPerUnit * sizeof(float2));
+  w.ticket_bytes = align(static_cast<size_t>(n_seqs) * L.n_kv * L.qchunks() * sizeof(int32_t));
   w.o_offset = w.plan_bytes;
   w.ml_offset = w.o_offset + w.o_bytes;
-  w.total = w.ml_offset + w.ml_bytes;
+  w.ticket_offset = w.ml_offset + w.ml_bytes;
+  w.total = w.ticket_offset + w.ticket_bytes;
   return w;
 }
 

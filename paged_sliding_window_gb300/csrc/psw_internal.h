@@ -36,10 +36,10 @@ cudaError_t device_info(DeviceInfo* info);
 // Per-device error word used by every kernel (device pointer).
 int32_t* device_error_word();
 
-// Decode workspace layout (bytes): plan | partial O | partial (m, l).
+// Decode workspace layout (bytes): plan | partial O | partial (m, l) | merge tickets.
 struct DecodeWorkspace {
-  size_t plan_bytes, o_bytes, ml_bytes, total;
-  size_t o_offset, ml_offset;
+  size_t plan_bytes, o_bytes, ml_bytes, ticket_bytes, total;
+  size_t o_offset, ml_offset, ticket_offset;
 };
 DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_ctas);
 

@@ -57,13 +57,14 @@ FULL = Layer(n_q_heads=32, n_kv_heads=4, head_dim=512, window=0, k_eq_v=True)
 
 
 def test_workspace_bytes_arithmetic(lib):
-    # (max CTAs + units) slots of 8 query heads x (head_dim floats + (m, l))
+    # plan + (max CTAs + units) slots of 8 query heads x (head_dim floats + (m, l)) + tickets
     def expect(layer, n_seqs):
         G = layer.n_q_heads // layer.n_kv_heads
         units = n_seqs * layer.n_kv_heads * ((G + 7) // 8)
         slots = 512 + units
         align = lambda x: (x + 255) // 256 * 256
-        return align((n_seqs + 1) * 16) + align(slots * 8 * layer.head_dim * 4) + align(slots * 8 * 8)
+        return (align((n_seqs + 1) * 16) + align(slots * 8 * layer.head_dim * 4) +
+                align(slots * 8 * 8) + align(units * 4))
     for layer, n in ((SLIDING, 64), (FULL, 32), (SLIDING, 0), (FULL, 1000)):
         assert binding.workspace_bytes(layer, n, 4096) == expect(layer, n)
 
