@@ -12,10 +12,10 @@
 //
 // Design (how, on sm_103a):
 //  * Work unit = (sequence, KV head, group of <= 8 query heads); a unit's
-//    visible pages are cut into tiles of 4 pages (64 keys). All tiles of all
-//    units form one list, planned on the device from seq_lens, and a
-//    persistent grid (one CTA per SM) takes equal contiguous slices of it, so
-//    the load is balanced whatever the length mix.
+//    visible pages are cut into tiles of 32 KB of K/V (2 pages at head_dim
+//    256). All tiles of all units form one list, planned on the device from
+//    seq_lens, and a persistent grid (two CTAs per SM) takes equal contiguous
+//    slices of it, so the load is balanced whatever the length mix.
 //  * Warp 4 is the producer: it reads block ids and issues one 2 KB TMA box
 //    per (page, 128-byte chunk of head_dim) into a 3-stage shared-memory ring
 //    (128-byte swizzle), completing on mbarriers.
@@ -55,27 +55,33 @@ struct SeqPlan {
   int32_t ntu;       // tiles per unit
 };
 
+// Two CTAs share each SM: every tile is 32 KB of K/V (2 pages of K and V, or
+// 4 pages of K alone with k_eq_v at head_dim 256, ...), 3 tiles in flight per
+// CTA, so each SM keeps two independent TMA pipelines and 8 consumer warps.
+constexpr int kCtasPerSm = 2;
+constexpr int kStageTarget = 32768;
+
 template <int HD, bool KEQV>
 struct Cfg {
   static constexpr int kChunks = HD / 64;
   static constexpr int kPageBytes = kChunks * kChunkBytes;
-  static constexpr int kTilePages = (HD == 512 && !KEQV) ? 2 : 4;
+  static constexpr int kTilePages = kStageTarget / (kPageBytes * (KEQV ? 1 : 2));
   static constexpr int kTileKeys = kTilePages * kBlockSize;
+  static constexpr int kSRow = kTileKeys < 32 ? 32 : kTileKeys;  // score-exchange row stride
   static constexpr int kKTileBytes = kTilePages * kPageBytes;
   static constexpr int kStageBytes = kKTileBytes * (KEQV ? 1 : 2);
-  static constexpr int kStagesFit = 196608 / kStageBytes;
-  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kStages = 3;
   static constexpr int kDPerWarp = HD / kConsumerWarps;
   static constexpr int kKSteps = kDPerWarp / 16;
   static constexpr int kMTiles = kDPerWarp / 16;
   static constexpr int kChunksPerWarp = kDPerWarp / 64;
-  static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kTileKeys;
+  static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kSRow;
   static constexpr int kTmaPerTile = kTilePages * kChunks * (KEQV ? 1 : 2);
   static constexpr int kSmemBytes =
       1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + 64;
+  static_assert(kTilePages >= 1, "tile of at least one page");
   static_assert(kTmaPerTile <= 32, "one TMA box per producer lane");
-  static_assert(kStages >= 2, "need a pipeline");
-  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory per SM");
 };
 
 // XOR swizzle of the key index in the score-exchange buffer: conflict-free
@@ -220,7 +226,7 @@ __device__ void merge_unit(int u, int c0, int c1, int nh, float* out_rows, float
 
 // ---------------------------------------------------------------- split
 template <int HD, bool KEQV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map,
                     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
@@ -417,15 +423,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     }
     float* sb = sbuf + (consumed & 1) * C::kSBufFloats;
     {
-      float* mine = sb + warp * kQHeadsPerUnit * C::kTileKeys;
+      float* mine = sb + warp * kQHeadsPerUnit * C::kSRow;
       #pragma unroll
       for (int mt = 0; mt < TP; ++mt) {
         const int k0 = mt * 16 + g;
         const int qa = 2 * t4, qb = 2 * t4 + 1;
-        mine[qa * C::kTileKeys + sbuf_key(qa, k0)] = sacc[mt][0];
-        mine[qb * C::kTileKeys + sbuf_key(qb, k0)] = sacc[mt][1];
-        mine[qa * C::kTileKeys + sbuf_key(qa, k0 + 8)] = sacc[mt][2];
-        mine[qb * C::kTileKeys + sbuf_key(qb, k0 + 8)] = sacc[mt][3];
+        mine[qa * C::kSRow + sbuf_key(qa, k0)] = sacc[mt][0];
+        mine[qb * C::kSRow + sbuf_key(qb, k0)] = sacc[mt][1];
+        mine[qa * C::kSRow + sbuf_key(qa, k0 + 8)] = sacc[mt][2];
+        mine[qb * C::kSRow + sbuf_key(qb, k0 + 8)] = sacc[mt][3];
       }
     }
     named_bar_sync(1, kConsumerWarps * 32);
@@ -446,7 +452,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         #pragma unroll
         for (int ww = 0; ww < kConsumerWarps; ++ww) {
           const float2 v2 = *reinterpret_cast<const float2*>(
-              sb + (ww * kQHeadsPerUnit + g) * C::kTileKeys + sbuf_key(g, key));
+              sb + (ww * kQHeadsPerUnit + g) * C::kSRow + sbuf_key(g, key));
           acc.x += v2.x;
           acc.y += v2.y;
         }
@@ -606,7 +612,7 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
            int n_seqs, float* out, float* lse, void* ws, size_t ws_bytes, int num_sms,
            int32_t* err, cudaStream_t stream) {
   using C = Cfg<HD, KEQV>;
-  const int grid = num_sms < kMaxDecodeCtas ? num_sms : kMaxDecodeCtas;
+  const int grid = num_sms * kCtasPerSm < kMaxDecodeCtas ? num_sms * kCtasPerSm : kMaxDecodeCtas;
   const DecodeWorkspace lay = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas);
   if (ws_bytes < lay.total) return PSW_EWORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(ws);
