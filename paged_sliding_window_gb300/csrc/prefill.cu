@@ -16,18 +16,27 @@
 // chunk tokens, half of head_dim for head_dim 512):
 //  * 128 query rows = (128/G tokens) x (G heads), token-major. Q is loaded once
 //    by TMA (128-byte swizzle, one box per 64 columns of head_dim).
-//  * Warp 4 (producer) streams K and V tiles of BN keys (64 for head_dim 256,
-//    32 for 512) into a 2-stage ring, one 2 KB TMA box per (page, 64-column
-//    chunk). Pages past the sequence end load as zeros (out-of-range box).
-//  * Warp 5 (one elected thread) issues tcgen05.mma: S = Q K^T (SS, both
-//    K-major) into TMEM, and O += P V (TS: P from TMEM, V MN-major from shared
-//    memory). QK of tile j+1 is issued before PV of tile j so the tensor pipe
-//    works while the softmax warps run.
-//  * Warps 0-3 (one thread per row) read S from TMEM, apply scale, softcap and
-//    the band/causal predicate, run the online softmax in fp32 (exp2 domain,
-//    lazy rescaling of O only when the running max grows by more than 2^8),
-//    and write P back to TMEM as a bf16 high part and a bf16 remainder; both
-//    are multiplied into O, so P enters the product to about 2^-17 relative.
+//  * Warps 8 (Q, K) and 10 (V) stream K and V tiles of BN keys (64 for
+//    head_dim 256, 32 for 512) into a 2-stage ring (1 stage for head_dim 512
+//    without k_eq_v, whose 128 KB Q tile leaves no room for two), one 2 KB TMA
+//    box per (page, 64-column chunk), and warm L2 with the tile two ahead. K
+//    and V of a stage are filled and released separately. Pages past the
+//    sequence end load as zeros.
+//  * Warp 9 (one elected thread) issues tcgen05.mma: S_j = Q K_j^T (SS, both
+//    K-major) into one of two S buffers in TMEM, and O += P_j V_j (TS: P from
+//    one of two P buffers in TMEM, V MN-major from shared memory). The issue
+//    order QK_0, QK_1, PV_0, QK_2, PV_1, ... keeps the tensor pipe fed while
+//    the softmax warps work on the tile before.
+//  * Warps 0-7 run the softmax. Warps w and w+4 own the same 32 rows (TMEM
+//    lanes 32 (w mod 4) ...) and split the BN key columns in halves; per tile
+//    they exchange one partial row maximum through shared memory. Scores get
+//    scale, softcap (odd polynomial on the FMA pipe for |s/cap| <= 1/2, the
+//    exp formula beyond) and, on band-edge tiles only, the band/causal
+//    predicate; the online softmax runs in fp32 in the exp2 domain with lazy
+//    rescaling of O (only when the running max grows by more than 2^8; the
+//    two warps of a row pair rescale half of O each). P is written back to
+//    TMEM as a bf16 high part and a bf16 remainder; both are multiplied into
+//    O, so P enters the product to about 2^-17 relative.
 //  * V rows of key positions that no row of the tile can see (before the
 //    window of the tile's first row, after its last row) are zeroed in shared
 //    memory so uncached or stale slots never reach O.
@@ -41,10 +50,11 @@
 namespace psw {
 namespace pf {
 
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;   // Q and K tiles
+constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10; // V tiles (idle with k_eq_v)
+constexpr int kThreads = 11 * 32;
 constexpr int kRows = 128;
 constexpr int kPageBoxBytes = kBlockSize * 128;  // one TMA box: 16 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
@@ -55,6 +65,7 @@ template <int HD, bool KEQV>
 struct Cfg {
   static constexpr int kQChunks = HD / 64;
   static constexpr int kBN = (HD == 256) ? 64 : 32;
+  static constexpr int kHalf = kBN / 2;  // key columns per softmax warp
   static constexpr int kPagesPerTile = kBN / kBlockSize;
   static constexpr int kOCols = 256;
   static constexpr int kDSplit = HD / kOCols;
@@ -64,35 +75,62 @@ struct Cfg {
   static constexpr int kKBytes = kQChunks * kChunkTileBytes;
   static constexpr int kVBytes = KEQV ? 0 : kVChunks * kChunkTileBytes;
   static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kStages = 2;
-  static constexpr int kSmemBytes = 1024 + kQBytes + kStages * kStageBytes + 256;
+  static constexpr int kBarsBytes = 4096;
+  // two K/V stages where they fit (head_dim 512 without k_eq_v gets one)
+  static constexpr int kStages =
+      (1024 + kQBytes + 2 * kStageBytes + kBarsBytes <= 232448) ? 2 : 1;
+  static constexpr int kSmemBytes = 1024 + kQBytes + kStages * kStageBytes + kBarsBytes;
+  // tensor memory columns: O | S0 | S1 | P0 (hi, lo) | P1 (hi, lo)
   static constexpr int kTmemO = 0;
-  static constexpr int kTmemS = 256;
-  static constexpr int kTmemPhi = 256 + kBN;
-  static constexpr int kTmemPlo = 256 + kBN + kBN / 2;
+  static constexpr int kTmemS = 256;                 // + b * kBN
+  static constexpr int kTmemP = 256 + 2 * kBN;       // + b * kBN; hi then lo (kBN/2 each)
   static constexpr int kTmemCols = 512;
   static constexpr int kTmaPerStage = kPagesPerTile * (kQChunks + (KEQV ? 0 : kVChunks));
   static_assert(kTmaPerStage <= 32, "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(kTmemPlo + kBN / 2 <= kTmemCols, "tensor memory columns");
+  static_assert(kTmemP + 2 * kBN <= kTmemCols, "tensor memory columns");
+  static_assert(!KEQV || kStages == 2, "k_eq_v keeps two stages");
 };
+
+template <int S>
+__device__ __forceinline__ int stage_of(int j) { return j % S; }
+template <int S>
+__device__ __forceinline__ uint32_t round_of(int j) { return static_cast<uint32_t>(j / S) & 1u; }
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
-  uint64_t s_full, s_free, p_full, pv_done, mma_drained;
+  // K and V parts of a stage are filled and released separately: K is free
+  // once QK has read it, V once PV has (with k_eq_v, V is the K part and the
+  // K part is released after PV). First kStages entries used.
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t mma_drained;
   uint32_t tmem_base;
   int abort;     // set by any warp; read by the producer and the MMA issuer
   int sm_abort;  // set only by softmax threads, read after their named barrier
+  float red_max[2][2][kRows];  // [tile parity][column half][row]
+  float red_sum[2][kRows];     // [column half][row]
 };
 
-// softcap: cap * tanh(x / cap) with tanh from one exp2 and one reciprocal.
-__device__ __forceinline__ float softcap_tanh(float x, float cap, float inv_cap) {
-  const float y = x * inv_cap;
-  const float t = exp2f(-2.f * kLog2e * fabsf(y));      // e^{-2|y|}
-  const float th = __fdividef(1.f - t, 1.f + t);         // tanh |y|
-  return cap * copysignf(th, y);
+// tanh(y) for |y| <= 1/2: odd Taylor polynomial through y^11 (the next term
+// is below 4.4e-7). Branch-free, FMA pipe only.
+__device__ __forceinline__ float tanh_small(float y) {
+  const float y2 = y * y;
+  float r = -1382.f / 155925.f;
+  r = fmaf(r, y2, 62.f / 2835.f);
+  r = fmaf(r, y2, -17.f / 315.f);
+  r = fmaf(r, y2, 2.f / 15.f);
+  r = fmaf(r, y2, -1.f / 3.f);
+  return fmaf(r * y2, y, y);
+}
+
+// tanh(y) for any y: 1 - 2 / (e^{2|y|} + 1) with the sign restored, the
+// polynomial where |y| <= 1/2 (where this form loses relative precision).
+__device__ __forceinline__ float tanh_any(float y) {
+  const float ay = fabsf(y);
+  const float t = ex2_approx(-2.f * kLog2e * ay);  // e^{-2|y|}
+  const float big = copysignf(__fdividef(1.f - t, 1.f + t), y);
+  return ay <= 0.5f ? tanh_small(y) : big;
 }
 
 template <int HD, bool KEQV>
@@ -105,6 +143,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                float* __restrict__ lse, int32_t* err) {
   using C = Cfg<HD, KEQV>;
   constexpr int BN = C::kBN;
+  constexpr int HALF = C::kHalf;
   const int T = kRows / group;  // chunk tokens per tile
   const int rb = blockIdx.x;
   const int kvh = blockIdx.y / C::kDSplit;
@@ -148,14 +187,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], kSoftmaxWarps);
+      mbar_init(&bars->p_full[i], kSoftmaxWarps);
+      mbar_init(&bars->p_free[i], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxWarps);
-    mbar_init(&bars->p_full, kSoftmaxWarps);
-    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->mma_drained, 1);
     bars->abort = 0;
     bars->sm_abort = 0;
@@ -171,9 +212,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
 
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    const bool v_side = (warp == kVProducerWarp);
+    if (v_side && KEQV) goto done;  // V is the K tile
+    if (!v_side && lane == 0) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
       if (!KEQV) prefetch_tensormap(&v_map);
@@ -183,54 +226,65 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         tma_load_3d(q_smem + c * (kRows * 128), &q_map, &bars->q_full, c * 64, kvh * group,
                     q0 + i0);
     }
-    // lane -> (page in tile, chunk, K or V)
-    const int per_page = C::kQChunks + (KEQV ? 0 : C::kVChunks);
-    const int lp = lane / per_page;
-    const int lc = lane - lp * per_page;
-    const bool is_v = lc >= C::kQChunks;
+    // K boxes: lane -> (page, chunk) for lane < pages * kQChunks; V boxes likewise
+    const int k_lp = lane / C::kQChunks, k_lc = lane - k_lp * C::kQChunks;
+    const int v_lp = lane / C::kVChunks, v_lc = lane - v_lp * C::kVChunks;
+    constexpr int kKBoxes = C::kPagesPerTile * C::kQChunks;
+    constexpr int kVBoxes = C::kPagesPerTile * C::kVChunks;
+    auto block_of = [&](int tile, int pp) -> int {  // physical block of page pp of key tile `tile`
+      const int page = tile * C::kPagesPerTile + pp;
+      if (page > last_page) return -1;
+      int blk = block_table[static_cast<int64_t>(b) * max_blocks + page];
+      if (blk < 0 || blk >= num_blocks) {
+        flag_error(err, PSW_DEVERR_BLOCK_ID);
+        blk = -1;  // out-of-range box: TMA fills zeros
+      }
+      return blk;
+    };
     int issued = 0;
     for (int j = 0; j < nkt; ++j, ++issued) {
-      const int stage = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      const int page0 = (kt0 + j) * C::kPagesPerTile;
-      int blk = -1;
-      if (lane < C::kPagesPerTile) {
-        const int page = page0 + lane;
-        if (page <= last_page) {
-          blk = block_table[static_cast<int64_t>(b) * max_blocks + page];
-          if (blk < 0 || blk >= num_blocks) {
-            flag_error(err, PSW_DEVERR_BLOCK_ID);
-            blk = -1;
-          }
-        }
-      }
-      const int my_blk = __shfl_sync(0xffffffffu, blk, lp < C::kPagesPerTile ? lp : 0);
+      const int stage = stage_of<C::kStages>(j);
+      const uint32_t ph = round_of<C::kStages>(j);
+      const int blk = (lane < C::kPagesPerTile) ? block_of(kt0 + j, lane) : -1;
+      const int blk_pf = (lane < C::kPagesPerTile && j + 2 < nkt) ? block_of(kt0 + j + 2, lane) : -1;
+      uint8_t* st = stages + stage * C::kStageBytes;
+      uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
+      uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&bars->kv_empty[stage], ph ^ 1);
+      if (lane == 0) ok = mbar_wait(empty, ph ^ 1);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok || *abort_flag) {
         if (lane == 0) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->kv_full[stage], C::kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, v_side ? C::kVBytes : C::kKBytes);
       __syncwarp();
-      if (lane < C::kTmaPerStage) {
-        uint8_t* st = stages + stage * C::kStageBytes;
-        if (!is_v) {
-          tma_load_3d(st + lc * C::kChunkTileBytes + lp * kPageBoxBytes, &k_map,
-                      &bars->kv_full[stage], 0, kvh * C::kQChunks + lc, my_blk * kBlockSize);
-        } else {
-          const int cv = lc - C::kQChunks;
-          tma_load_3d(st + C::kKBytes + cv * C::kChunkTileBytes + lp * kPageBoxBytes, &v_map,
-                      &bars->kv_full[stage], 0, kvh * C::kQChunks + dh * C::kVChunks + cv,
-                      my_blk * kBlockSize);
+      if (!v_side) {
+        const int kb_blk = __shfl_sync(0xffffffffu, blk, k_lp < C::kPagesPerTile ? k_lp : 0);
+        const int kp_blk = __shfl_sync(0xffffffffu, blk_pf, k_lp < C::kPagesPerTile ? k_lp : 0);
+        if (lane < kKBoxes) {
+          tma_load_3d(st + k_lc * C::kChunkTileBytes + k_lp * kPageBoxBytes, &k_map, full, 0,
+                      kvh * C::kQChunks + k_lc, kb_blk * kBlockSize);
+          if (j + 2 < nkt && kp_blk >= 0)  // warm L2 with the tile two ahead
+            tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, kp_blk * kBlockSize);
+        }
+      } else {
+        const int vb_blk = __shfl_sync(0xffffffffu, blk, v_lp < C::kPagesPerTile ? v_lp : 0);
+        const int vp_blk = __shfl_sync(0xffffffffu, blk_pf, v_lp < C::kPagesPerTile ? v_lp : 0);
+        if (lane < kVBoxes) {
+          const int y = kvh * C::kQChunks + dh * C::kVChunks + v_lc;
+          tma_load_3d(st + C::kKBytes + v_lc * C::kChunkTileBytes + v_lp * kPageBoxBytes, &v_map,
+                      full, 0, y, vb_blk * kBlockSize);
+          if (j + 2 < nkt && vp_blk >= 0) tma_prefetch_3d(&v_map, 0, y, vp_blk * kBlockSize);
         }
       }
     }
-    if (lane == 0) {  // drain this CTA's own copies before anyone leaves
-      mbar_wait(&bars->q_full, 0);
+    if (lane == 0) {  // drain this warp's own copies before anyone leaves
+      if (!v_side) mbar_wait(&bars->q_full, 0);
       for (int i = max(0, issued - C::kStages); i < issued; ++i)
-        mbar_wait(&bars->kv_full[i & 1], (i >> 1) & 1);
+        mbar_wait(v_side ? &bars->v_full[stage_of<C::kStages>(i)]
+                         : &bars->k_full[stage_of<C::kStages>(i)],
+                  round_of<C::kStages>(i));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -240,27 +294,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const uint32_t q_base = smem_u32(q_smem);
       const uint32_t st_base = smem_u32(stages);
       bool ok = mbar_wait(&bars->q_full, 0);
-      auto issue_pv = [&](int jj) {
-        const uint32_t kb = st_base + (jj & 1) * C::kStageBytes;
+      auto issue_pv = [&](int i) -> bool {
+        const int pb = i & 1;
+        if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1) || *abort_flag) return false;
+        if (!KEQV && !mbar_wait(&bars->v_full[stage_of<C::kStages>(i)], round_of<C::kStages>(i)))
+          return false;
+        tc::fence_after();
+        const uint32_t kb = st_base + stage_of<C::kStages>(i) * C::kStageBytes;
         const uint32_t vb = KEQV ? kb + dh * C::kVChunks * C::kChunkTileBytes : kb + C::kKBytes;
+        const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
         #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks) {
           const uint64_t bdesc = tc::smem_desc(vb + ks * 16 * 128, C::kChunkTileBytes, 1024,
                                                tc::kSwizzle128B);
-          tc::mma_ts(tmem + C::kTmemO, tmem + C::kTmemPhi + ks * 8, bdesc, idesc_pv,
-                     (jj > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_ts(tmem + C::kTmemO, tmem + C::kTmemPlo + ks * 8, bdesc, idesc_pv, 1u);
+          tc::mma_ts(tmem + C::kTmemO, p_hi + ks * 8, bdesc, idesc_pv,
+                     (i > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ts(tmem + C::kTmemO, p_hi + BN / 2 + ks * 8, bdesc, idesc_pv, 1u);
         }
-        tc::commit(&bars->pv_done);
-        tc::commit(&bars->kv_empty[jj & 1]);
+        tc::commit(&bars->p_free[pb]);
+        // V (or, with k_eq_v, the whole K part) of this stage is free once PV ends
+        tc::commit(KEQV ? &bars->k_empty[stage_of<C::kStages>(i)]
+                        : &bars->v_empty[stage_of<C::kStages>(i)]);
+        return true;
       };
       int j = 0;
       for (; ok && j < nkt; ++j) {
-        ok = mbar_wait(&bars->kv_full[j & 1], (j >> 1) & 1);
-        if (ok && j > 0) ok = mbar_wait(&bars->s_free, (j - 1) & 1);
+        const int sb = j & 1;
+        ok = mbar_wait(&bars->k_full[stage_of<C::kStages>(j)], round_of<C::kStages>(j));
+        if (ok && j >= 2) ok = mbar_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1);
         if (!ok || *abort_flag) break;
         tc::fence_after();
-        const uint32_t kb = st_base + (j & 1) * C::kStageBytes;
+        const uint32_t kb = st_base + stage_of<C::kStages>(j) * C::kStageBytes;
         #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const int c = ks >> 2;
@@ -268,23 +332,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                                                1024, tc::kSwizzle128B);
           const uint64_t bdesc = tc::smem_desc(kb + c * C::kChunkTileBytes + (ks & 3) * 32, 16,
                                                1024, tc::kSwizzle128B);
-          tc::mma_ss(tmem + C::kTmemS, adesc, bdesc, idesc_qk, ks > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + C::kTmemS + sb * BN, adesc, bdesc, idesc_qk, ks > 0 ? 1u : 0u);
         }
-        tc::commit(&bars->s_full);
-        if (j > 0) {
-          ok = mbar_wait(&bars->p_full, (j - 1) & 1);
-          if (!ok || *abort_flag) break;
-          tc::fence_after();
-          issue_pv(j - 1);
-        }
+        tc::commit(&bars->s_full[sb]);
+        if (!KEQV) tc::commit(&bars->k_empty[stage_of<C::kStages>(j)]);  // K read by QK
+        if (j > 0) ok = issue_pv(j - 1);
       }
-      if (ok && j == nkt && !*abort_flag) {
-        ok = mbar_wait(&bars->p_full, (nkt - 1) & 1);
-        if (ok) {
-          tc::fence_after();
-          issue_pv(nkt - 1);
-        }
-      }
+      if (ok && j == nkt && !*abort_flag) ok = issue_pv(nkt - 1);
       if (!ok) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
       // every MMA this thread issued has finished before tensor memory is freed
       tc::commit(&bars->mma_drained);
@@ -293,83 +347,119 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = warp * 32 + lane;
+    const int quad = warp & 3;       // TMEM lane quadrant = rows 32*quad ...
+    const int half = warp >> 2;      // key columns [half*HALF, (half+1)*HALF)
+    const int r = quad * 32 + lane;  // tile row
     const int t = r / group;
     const int h = r - t * group;
     const bool row_ok = (t < tok_valid) && (r < group * T);
     const int p = past + i0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + C::kTmemS;
-    const uint32_t t_o = tmem + lane_off + C::kTmemO;
+    const int vis_lo = (window > 0) ? max(0, p - window + 1) : 0;  // this row sees [vis_lo, p]
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool use_cap = softcap > 0.f;
     const float inv_cap = use_cap ? 1.f / softcap : 0.f;
+    const float cap_l2 = softcap * kLog2e;
     const float scale_l2 = scale * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
-    volatile int* sm_abort = &bars->sm_abort;  // written only by softmax threads
+    volatile int* sm_abort = &bars->sm_abort;
+    const uint32_t pair_bar = 1 + quad;  // named barrier of warps quad and quad + 4
     for (int j = 0; j < nkt; ++j) {
+      const int sb = j & 1;
       // every decision below is warp-uniform; the abort decision is taken by all
-      // four softmax warps together after the named barrier
-      bool okw = __all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1));
-      float x[BN];
-      const int key0 = (kt0 + j) * BN;
+      // softmax warps together after the named barrier at the end of the tile
+      bool okw = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1));
+      const int key0 = (kt0 + j) * BN + half * HALF;
+      float x[HALF];
       float alpha = 1.f;
       if (okw) {
         tc::fence_after();
-        #pragma unroll
-        for (int c16 = 0; c16 < BN / 16; ++c16) {
-          uint32_t v[16];
-          tc::ld16(t_s + c16 * 16, v);
+        {
+          uint32_t v[HALF];
+          #pragma unroll
+          for (int c16 = 0; c16 < HALF / 16; ++c16)
+            tc::ld16(tmem + lane_off + C::kTmemS + sb * BN + half * HALF + c16 * 16,
+                     *reinterpret_cast<uint32_t(*)[16]>(&v[c16 * 16]));
           tc::wait_ld();
           #pragma unroll
-          for (int i = 0; i < 16; ++i) x[c16 * 16 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < HALF; ++i) x[i] = __uint_as_float(v[i]);
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free);
+        if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-        // scale, softcap, band + causal predicate, tile max
-        float mx = -INFINITY;
-        #pragma unroll
-        for (int k = 0; k < BN; ++k) {
-          const int key = key0 + k;
-          float v = x[k];
-          v = use_cap ? softcap_tanh(v * scale, softcap, inv_cap) * kLog2e : v * scale_l2;
-          const bool vis = row_ok && key <= p && (window == 0 || p - key < window);
-          v = vis ? v : -INFINITY;
-          x[k] = v;
-          mx = fmaxf(mx, v);
-        }
-        const float m_cand = fmaxf(m_run, mx);
-        if (m_cand > m_run + kRescaleThreshold) {  // lazy rescale (also the first visible key)
-          alpha = exp2f(m_run - m_cand);
-          m_run = m_cand;
-        }
-      }
-      // P_{j-1} has been multiplied in and O is stable once PV_{j-1} is done
-      if (okw && j > 0) {
-        okw = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (j - 1) & 1));
-        tc::fence_after();
-        if (okw && __any_sync(0xffffffffu, alpha != 1.f)) {
-          #pragma unroll 1
-          for (int c16 = 0; c16 < C::kOCols / 16; ++c16) {
-            uint32_t v[16];
-            tc::ld16(t_o + c16 * 16, v);
-            tc::wait_ld();
-            #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tc::st16(t_o + c16 * 16, v);
+        // scale (+ softcap) into the exp2 domain; every loop is branch-free
+        if (use_cap) {
+          const float sc = scale * inv_cap;
+          bool big = false;
+          #pragma unroll
+          for (int k = 0; k < HALF; ++k) {
+            x[k] *= sc;
+            big |= fabsf(x[k]) > 0.5f;
           }
-          tc::wait_st();
+          if (__any_sync(0xffffffffu, big)) {
+            #pragma unroll
+            for (int k = 0; k < HALF; ++k) x[k] = cap_l2 * tanh_any(x[k]);
+          } else {
+            #pragma unroll
+            for (int k = 0; k < HALF; ++k) x[k] = cap_l2 * tanh_small(x[k]);
+          }
+        } else {
+          #pragma unroll
+          for (int k = 0; k < HALF; ++k) x[k] *= scale_l2;
+        }
+        // band + causal predicate only where the tile straddles this row's edges
+        const bool interior = row_ok && key0 >= vis_lo && key0 + HALF - 1 <= p;
+        if (!__all_sync(0xffffffffu, interior)) {
+          #pragma unroll
+          for (int k = 0; k < HALF; ++k) {
+            const int key = key0 + k;
+            x[k] = (row_ok && key >= vis_lo && key <= p) ? x[k] : -INFINITY;
+          }
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        #pragma unroll
+        for (int k = 0; k < HALF; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+        bars->red_max[sb][half][r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
+      named_bar_sync(pair_bar, 64);  // the two halves of these rows meet
+      if (okw) {
+        const float m_tile = fmaxf(bars->red_max[sb][0][r], bars->red_max[sb][1][r]);
+        if (m_tile > m_run + kRescaleThreshold) {  // lazy rescale (also the first visible key)
+          alpha = ex2_approx(m_run - m_tile);
+          m_run = m_tile;
+        }
+        // rescaling O needs PV_{j-1} finished; each warp of the pair takes half of O
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          okw = __all_sync(0xffffffffu,
+                           mbar_wait(&bars->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          tc::fence_after();
+          if (okw) {
+            #pragma unroll 1
+            for (int c16 = 0; c16 < C::kOCols / 32; ++c16) {
+              const uint32_t col = tmem + lane_off + C::kTmemO + half * (C::kOCols / 2) + c16 * 16;
+              uint32_t v[16];
+              tc::ld16(col, v);
+              tc::wait_ld();
+              #pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tc::st16(col, v);
+            }
+            tc::wait_st();
+          }
         }
       }
       if (okw) {
         // zero V rows that no row of this tile can see (first / last key tile)
         if (j == 0 || j == nkt - 1) {
-          uint8_t* st = stages + (j & 1) * C::kStageBytes;
+          const int tkey0 = (kt0 + j) * BN;
+          uint8_t* st = stages + stage_of<C::kStages>(j) * C::kStageBytes;
           uint8_t* vt = KEQV ? st + dh * C::kVChunks * C::kChunkTileBytes : st + C::kKBytes;
-          const int z_lo = max(0, j_lo - key0);       // rows [0, z_lo) hidden
-          const int z_hi = min(BN, j_hi - key0 + 1);  // rows [z_hi, BN) hidden
-          if (z_lo > 0 || z_hi < BN) {
+          const int z_lo = max(0, j_lo - tkey0);       // rows [0, z_lo) hidden
+          const int z_hi = min(BN, j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
+          if (!KEQV && (z_lo > 0 || z_hi < BN))  // V may land after K
+            okw = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[stage_of<C::kStages>(j)],
+                                                    round_of<C::kStages>(j)));
+          if (okw && (z_lo > 0 || z_hi < BN)) {
             for (int idx = threadIdx.x; idx < C::kVChunks * BN * 8; idx += kSoftmaxWarps * 32) {
               const int cv = idx / (BN * 8);
               const int rem = idx - cv * (BN * 8);
@@ -381,25 +471,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             fence_proxy_async_smem();
           }
         }
-        // P = exp2(x - m): bf16 high part and bf16 remainder into tensor memory
+        // P_{j-2} must have been multiplied in before its buffer is rewritten
+        if (j >= 2)
+          okw = __all_sync(0xffffffffu,
+                           mbar_wait(&bars->p_free[sb], ((j >> 1) - 1) & 1));
+      }
+      if (okw) {
+        // P = 2^(x - m): bf16 high part and bf16 remainder into tensor memory
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float psum = 0.f;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t hi[HALF / 2], lo[HALF / 2];
         #pragma unroll
-        for (int c32 = 0; c32 < BN / 32; ++c32) {
-          uint32_t hi[16], lo[16];
-          #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = exp2f(x[c32 * 32 + 2 * i] - m_use);
-            const float bb = exp2f(x[c32 * 32 + 2 * i + 1] - m_use);
-            psum += a + bb;
-            hi[i] = pack_bf16x2(a, bb);
-            const float2 hf = unpack_bf16x2(hi[i]);
-            lo[i] = pack_bf16x2(a - hf.x, bb - hf.y);
-          }
-          tc::st16(tmem + lane_off + C::kTmemPhi + c32 * 16, hi);
-          tc::st16(tmem + lane_off + C::kTmemPlo + c32 * 16, lo);
+        for (int i = 0; i < HALF / 2; ++i) {
+          const float a = ex2_approx(x[2 * i] - m_use);
+          const float bb = ex2_approx(x[2 * i + 1] - m_use);
+          ps[i & 3] += a + bb;
+          hi[i] = pack_bf16x2(a, bb);
+          const float2 hf = unpack_bf16x2(hi[i]);
+          lo[i] = pack_bf16x2(a - hf.x, bb - hf.y);
         }
-        l_run = l_run * alpha + psum;
+        const uint32_t pcol = tmem + lane_off + C::kTmemP + sb * BN + half * (HALF / 2);
+        if constexpr (HALF / 2 == 16) {
+          tc::st16(pcol, hi);
+          tc::st16(pcol + BN / 2, lo);
+        } else {
+          tc::st8(pcol, hi);
+          tc::st8(pcol + BN / 2, lo);
+        }
+        l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
         tc::wait_st();
         tc::fence_before();
       }
@@ -407,23 +506,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         flag_error(err, PSW_DEVERR_PIPELINE);
         *sm_abort = 1;
       }
-      named_bar_sync(1, kSoftmaxWarps * 32);  // V zeroing of all softmax threads done
+      named_bar_sync(9, kSoftmaxWarps * 32);  // all softmax warps: V zeroing done, abort agreed
       if (*sm_abort) break;
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) mbar_arrive(&bars->p_full[sb]);
     }
     bool ok = !*sm_abort;
 
-    // epilogue: O / l to global, lse
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->pv_done, (nkt - 1) & 1));
+    // epilogue: l from both halves, O / l to global, lse
+    bars->red_sum[half][r] = l_run;
+    if (ok) ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->p_free[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1));
+    named_bar_sync(pair_bar, 64);
     tc::fence_after();
     if (ok) {
-      const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const float l_tot = bars->red_sum[0][r] + bars->red_sum[1][r];
+      const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
       float* orow = out + (static_cast<int64_t>(q0 + i0 + t) * n_q + kvh * group + h) * HD +
-                    dh * C::kOCols;
+                    dh * C::kOCols + half * (C::kOCols / 2);
       #pragma unroll 1
-      for (int c16 = 0; c16 < C::kOCols / 16; ++c16) {
+      for (int c16 = 0; c16 < C::kOCols / 32; ++c16) {
         uint32_t v[16];
-        tc::ld16(t_o + c16 * 16, v);
+        tc::ld16(tmem + lane_off + C::kTmemO + half * (C::kOCols / 2) + c16 * 16, v);
         tc::wait_ld();
         if (row_ok) {
           #pragma unroll
@@ -433,15 +536,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                             __uint_as_float(v[i + 2]) * inv_l, __uint_as_float(v[i + 3]) * inv_l);
         }
       }
-      if (row_ok && dh == 0 && lse != nullptr)
+      if (row_ok && dh == 0 && half == 0 && lse != nullptr)
         lse[static_cast<int64_t>(q0 + i0 + t) * n_q + kvh * group + h] =
-            (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            (l_tot > 0.f) ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
     } else if (lane == 0) {
       flag_error(err, PSW_DEVERR_PIPELINE);
       *abort_flag = 1;  // stops the producer and the MMA issuer
     }
   }
 
+done:
   tc::fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
