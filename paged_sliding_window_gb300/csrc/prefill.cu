@@ -17,11 +17,11 @@
 //  * 128 query rows = (128/G tokens) x (G heads), token-major. Q is loaded once
 //    by TMA (128-byte swizzle, one box per 64 columns of head_dim).
 //  * Warps 8 (Q, K) and 10 (V) stream K and V tiles of BN keys (64 for
-//    head_dim 256, 32 for 512) into a 2-stage ring (1 stage for head_dim 512
-//    without k_eq_v, whose 128 KB Q tile leaves no room for two), one 2 KB TMA
-//    box per (page, 64-column chunk), and warm L2 with the tile two ahead. K
-//    and V of a stage are filled and released separately. Pages past the
-//    sequence end load as zeros.
+//    head_dim 256, 32 for 512) into rings of their own (3 K and 2 V stages
+//    where shared memory allows), one 2 KB TMA box per (page, 64-column
+//    chunk), and warm L2 with the tile three ahead. A K stage is released as
+//    soon as QK has read it, a V stage after PV. Pages past the sequence end
+//    load as zeros.
 //  * Warp 9 (one elected thread) issues tcgen05.mma: S_j = Q K_j^T (SS, both
 //    K-major) into one of two S buffers in TMEM, and O += P_j V_j (TS: P from
 //    one of two P buffers in TMEM, V MN-major from shared memory). The issue
@@ -35,8 +35,9 @@
 //    predicate; the online softmax runs in fp32 in the exp2 domain with lazy
 //    rescaling of O (only when the running max grows by more than 2^8; the
 //    two warps of a row pair rescale half of O each). P is written back to
-//    TMEM as a bf16 high part and a bf16 remainder; both are multiplied into
-//    O, so P enters the product to about 2^-17 relative.
+//    TMEM as a bf16 high part and a bf16 remainder, split with integer ops
+//    (no conversion instructions); both are multiplied into O, so P enters the
+//    product to 2^-14 relative.
 //  * V rows of key positions that no row of the tile can see (before the
 //    window of the tile's first row, after its last row) are zeroed in shared
 //    memory so uncached or stale slots never reach O.
@@ -74,12 +75,16 @@ struct Cfg {
   static constexpr int kChunkTileBytes = kBN * 128;  // one 64-column chunk of a K/V tile
   static constexpr int kKBytes = kQChunks * kChunkTileBytes;
   static constexpr int kVBytes = KEQV ? 0 : kVChunks * kChunkTileBytes;
-  static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kBarsBytes = 4096;
-  // two K/V stages where they fit (head_dim 512 without k_eq_v gets one)
-  static constexpr int kStages =
-      (1024 + kQBytes + 2 * kStageBytes + kBarsBytes <= 232448) ? 2 : 1;
-  static constexpr int kSmemBytes = 1024 + kQBytes + kStages * kStageBytes + kBarsBytes;
+  static constexpr int kBarsBytes = 1536;
+  static constexpr int kBudget = 232448 - 1024 - kQBytes - kBarsBytes;
+  // K and V have rings of their own: K is consumed early (QK), V late (PV).
+  // Three K stages where they fit (two for head_dim 512 without k_eq_v), two
+  // V stages (one when only that fits).
+  static constexpr int kKStages = (3 * kKBytes + 2 * kVBytes <= kBudget) ? 3 : 2;
+  static constexpr int kVStages = KEQV ? 0 : ((kKStages * kKBytes + 2 * kVBytes <= kBudget) ? 2 : 1);
+  static constexpr int kSmemBytes =
+      1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kBarsBytes;
+  static constexpr int kVS = kVStages > 0 ? kVStages : 1;  // ring size for index math
   // tensor memory columns: O | S0 | S1 | P0 (hi, lo) | P1 (hi, lo)
   static constexpr int kTmemO = 0;
   static constexpr int kTmemS = 256;                 // + b * kBN
@@ -89,7 +94,7 @@ struct Cfg {
   static_assert(kTmaPerStage <= 32, "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kTmemP + 2 * kBN <= kTmemCols, "tensor memory columns");
-  static_assert(!KEQV || kStages == 2, "k_eq_v keeps two stages");
+  static_assert(kKStages * kKBytes + kVStages * kVBytes <= kBudget, "K/V rings");
 };
 
 template <int S>
@@ -99,17 +104,16 @@ __device__ __forceinline__ uint32_t round_of(int j) { return static_cast<uint32_
 
 struct Bars {
   uint64_t q_full;
-  // K and V parts of a stage are filled and released separately: K is free
-  // once QK has read it, V once PV has (with k_eq_v, V is the K part and the
-  // K part is released after PV). First kStages entries used.
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  // K and V rings are filled and released separately: a K stage is free once
+  // QK has read it, a V stage once PV has (with k_eq_v, V is the K stage and
+  // it is released after PV). First kKStages / kVStages entries used.
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t mma_drained;
   uint32_t tmem_base;
   int abort;     // set by any warp; read by the producer and the MMA issuer
   int sm_abort;  // set only by softmax threads, read after their named barrier
-  float red_max[2][2][kRows];  // [tile parity][column half][row]
-  float red_sum[2][kRows];     // [column half][row]
+  float red[2][kRows];  // [column half][row]: partial row max per tile, then row sums
 };
 
 // tanh(y) for |y| <= 1/2: odd Taylor polynomial through y^11 (the next term
@@ -122,6 +126,17 @@ __device__ __forceinline__ float tanh_small(float y) {
   r = fmaf(r, y2, 2.f / 15.f);
   r = fmaf(r, y2, -1.f / 3.f);
   return fmaf(r * y2, y, y);
+}
+
+// tanh_small on a pair of values (packed fp32 arithmetic).
+__device__ __forceinline__ uint64_t tanh_small2(uint64_t y) {
+  const uint64_t y2 = f2_mul(y, y);
+  uint64_t r = f2_fma(f2_pack(-1382.f / 155925.f, -1382.f / 155925.f), y2,
+                      f2_pack(62.f / 2835.f, 62.f / 2835.f));
+  r = f2_fma(r, y2, f2_pack(-17.f / 315.f, -17.f / 315.f));
+  r = f2_fma(r, y2, f2_pack(2.f / 15.f, 2.f / 15.f));
+  r = f2_fma(r, y2, f2_pack(-1.f / 3.f, -1.f / 3.f));
+  return f2_fma(f2_mul(r, y2), y, y);
 }
 
 // tanh(y) for any y: 1 - 2 / (e^{2|y|} + 1) with the sign restored, the
@@ -182,14 +197,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* q_smem = smem;
-  uint8_t* stages = smem + C::kQBytes;
-  Bars* bars = reinterpret_cast<Bars*>(stages + C::kStages * C::kStageBytes);
+  uint8_t* k_ring = smem + C::kQBytes;
+  uint8_t* v_ring = k_ring + C::kKStages * C::kKBytes;
+  Bars* bars = reinterpret_cast<Bars*>(v_ring + C::kVStages * C::kVBytes);
+  static_assert(sizeof(Bars) <= C::kBarsBytes, "barrier block");
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
@@ -231,9 +250,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int v_lp = lane / C::kVChunks, v_lc = lane - v_lp * C::kVChunks;
     constexpr int kKBoxes = C::kPagesPerTile * C::kQChunks;
     constexpr int kVBoxes = C::kPagesPerTile * C::kVChunks;
-    auto block_of = [&](int tile, int pp) -> int {  // physical block of page pp of key tile `tile`
-      const int page = tile * C::kPagesPerTile + pp;
-      if (page > last_page) return -1;
+    // Block ids of this CTA's pages, 32 at a time: lane l holds page
+    // first_page + 32 g + l of group g; the next group is loaded one group
+    // ahead, so a tile needs only shuffles.
+    constexpr int P = C::kPagesPerTile;
+    constexpr int kTilesPerGroup = 32 / P;
+    const int first_page = kt0 * P;
+    auto load_group = [&](int grp) -> int {
+      const int page = first_page + grp * 32 + lane;
+      if (grp * kTilesPerGroup >= nkt || page > last_page) return -1;
       int blk = block_table[static_cast<int64_t>(b) * max_blocks + page];
       if (blk < 0 || blk >= num_blocks) {
         flag_error(err, PSW_DEVERR_BLOCK_ID);
@@ -241,13 +266,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       }
       return blk;
     };
+    int ids = load_group(0), ids_next = load_group(1);
+    const int nst = v_side ? C::kVS : C::kKStages;
+    const int my_lp = v_side ? v_lp : k_lp;
     int issued = 0;
     for (int j = 0; j < nkt; ++j, ++issued) {
-      const int stage = stage_of<C::kStages>(j);
-      const uint32_t ph = round_of<C::kStages>(j);
-      const int blk = (lane < C::kPagesPerTile) ? block_of(kt0 + j, lane) : -1;
-      const int blk_pf = (lane < C::kPagesPerTile && j + 2 < nkt) ? block_of(kt0 + j + 2, lane) : -1;
-      uint8_t* st = stages + stage * C::kStageBytes;
+      const int stage = j % nst;
+      const uint32_t ph = static_cast<uint32_t>(j / nst) & 1u;
+      if (j > 0 && j % kTilesPerGroup == 0) {
+        ids = ids_next;
+        ids_next = load_group(j / kTilesPerGroup + 1);
+      }
+      const int src = (j % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
+      const int my_blk = __shfl_sync(0xffffffffu, ids, src);
+      const int jp = j + 3;  // tile whose pages are warmed in L2 now
+      const int psrc = (jp % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
+      const int pf_same = __shfl_sync(0xffffffffu, ids, psrc);
+      const int pf_next = __shfl_sync(0xffffffffu, ids_next, psrc);
+      const int pf_blk = (jp / kTilesPerGroup == j / kTilesPerGroup) ? pf_same : pf_next;
       uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
       uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
       bool ok = true;
@@ -260,31 +296,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       if (lane == 0) mbar_arrive_expect_tx(full, v_side ? C::kVBytes : C::kKBytes);
       __syncwarp();
       if (!v_side) {
-        const int kb_blk = __shfl_sync(0xffffffffu, blk, k_lp < C::kPagesPerTile ? k_lp : 0);
-        const int kp_blk = __shfl_sync(0xffffffffu, blk_pf, k_lp < C::kPagesPerTile ? k_lp : 0);
         if (lane < kKBoxes) {
-          tma_load_3d(st + k_lc * C::kChunkTileBytes + k_lp * kPageBoxBytes, &k_map, full, 0,
-                      kvh * C::kQChunks + k_lc, kb_blk * kBlockSize);
-          if (j + 2 < nkt && kp_blk >= 0)  // warm L2 with the tile two ahead
-            tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, kp_blk * kBlockSize);
+          tma_load_3d(k_ring + stage * C::kKBytes + k_lc * C::kChunkTileBytes +
+                          k_lp * kPageBoxBytes,
+                      &k_map, full, 0, kvh * C::kQChunks + k_lc, my_blk * kBlockSize);
+          if (jp < nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
+            tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, pf_blk * kBlockSize);
         }
       } else {
-        const int vb_blk = __shfl_sync(0xffffffffu, blk, v_lp < C::kPagesPerTile ? v_lp : 0);
-        const int vp_blk = __shfl_sync(0xffffffffu, blk_pf, v_lp < C::kPagesPerTile ? v_lp : 0);
         if (lane < kVBoxes) {
           const int y = kvh * C::kQChunks + dh * C::kVChunks + v_lc;
-          tma_load_3d(st + C::kKBytes + v_lc * C::kChunkTileBytes + v_lp * kPageBoxBytes, &v_map,
-                      full, 0, y, vb_blk * kBlockSize);
-          if (j + 2 < nkt && vp_blk >= 0) tma_prefetch_3d(&v_map, 0, y, vp_blk * kBlockSize);
+          tma_load_3d(v_ring + stage * C::kVBytes + v_lc * C::kChunkTileBytes +
+                          v_lp * kPageBoxBytes,
+                      &v_map, full, 0, y, my_blk * kBlockSize);
+          if (jp < nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, y, pf_blk * kBlockSize);
         }
       }
     }
     if (lane == 0) {  // drain this warp's own copies before anyone leaves
       if (!v_side) mbar_wait(&bars->q_full, 0);
-      for (int i = max(0, issued - C::kStages); i < issued; ++i)
-        mbar_wait(v_side ? &bars->v_full[stage_of<C::kStages>(i)]
-                         : &bars->k_full[stage_of<C::kStages>(i)],
-                  round_of<C::kStages>(i));
+      for (int i = max(0, issued - nst); i < issued; ++i)
+        mbar_wait(v_side ? &bars->v_full[i % nst] : &bars->k_full[i % nst],
+                  static_cast<uint32_t>(i / nst) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -292,53 +325,70 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, BN, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, C::kOCols, 0, 1);
       const uint32_t q_base = smem_u32(q_smem);
-      const uint32_t st_base = smem_u32(stages);
+      const uint32_t k_base = smem_u32(k_ring);
+      const uint32_t v_base = smem_u32(v_ring);
       bool ok = mbar_wait(&bars->q_full, 0);
-      auto issue_pv = [&](int i) -> bool {
-        const int pb = i & 1;
-        if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1) || *abort_flag) return false;
-        if (!KEQV && !mbar_wait(&bars->v_full[stage_of<C::kStages>(i)], round_of<C::kStages>(i)))
-          return false;
-        tc::fence_after();
-        const uint32_t kb = st_base + stage_of<C::kStages>(i) * C::kStageBytes;
-        const uint32_t vb = KEQV ? kb + dh * C::kVChunks * C::kChunkTileBytes : kb + C::kKBytes;
-        const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
-        #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bdesc = tc::smem_desc(vb + ks * 16 * 128, C::kChunkTileBytes, 1024,
-                                               tc::kSwizzle128B);
-          tc::mma_ts(tmem + C::kTmemO, p_hi + ks * 8, bdesc, idesc_pv,
-                     (i > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_ts(tmem + C::kTmemO, p_hi + BN / 2 + ks * 8, bdesc, idesc_pv, 1u);
+      // Non-blocking scheduler: issue QK_j as soon as K_j has landed and its S
+      // buffer is free (at most two ahead of the softmax), PV_i as soon as P_i
+      // is in TMEM and V_i has landed; QK first, so S is ready before the
+      // softmax asks for it. The tensor pipe runs the MMAs in issue order.
+      int next_qk = 0, next_pv = 0;
+      long long idle_since = clock64();
+      while (ok && next_pv < nkt) {
+        bool progressed = false;
+        if (next_qk < nkt && next_qk < next_pv + 2) {
+          const int j = next_qk, sb = j & 1;
+          if (mbar_try_wait(&bars->k_full[stage_of<C::kKStages>(j)], round_of<C::kKStages>(j)) &&
+              (j < 2 || mbar_try_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1))) {
+            tc::fence_after();
+            const uint32_t kb = k_base + stage_of<C::kKStages>(j) * C::kKBytes;
+            #pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              const int c = ks >> 2;
+              const uint64_t adesc = tc::smem_desc(q_base + c * (kRows * 128) + (ks & 3) * 32,
+                                                   16, 1024, tc::kSwizzle128B);
+              const uint64_t bdesc = tc::smem_desc(kb + c * C::kChunkTileBytes + (ks & 3) * 32,
+                                                   16, 1024, tc::kSwizzle128B);
+              tc::mma_ss(tmem + C::kTmemS + sb * BN, adesc, bdesc, idesc_qk, ks > 0 ? 1u : 0u);
+            }
+            tc::commit(&bars->s_full[sb]);
+            if (!KEQV) tc::commit(&bars->k_empty[stage_of<C::kKStages>(j)]);  // K read by QK
+            ++next_qk;
+            progressed = true;
+          }
         }
-        tc::commit(&bars->p_free[pb]);
-        // V (or, with k_eq_v, the whole K part) of this stage is free once PV ends
-        tc::commit(KEQV ? &bars->k_empty[stage_of<C::kStages>(i)]
-                        : &bars->v_empty[stage_of<C::kStages>(i)]);
-        return true;
-      };
-      int j = 0;
-      for (; ok && j < nkt; ++j) {
-        const int sb = j & 1;
-        ok = mbar_wait(&bars->k_full[stage_of<C::kStages>(j)], round_of<C::kStages>(j));
-        if (ok && j >= 2) ok = mbar_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1);
-        if (!ok || *abort_flag) break;
-        tc::fence_after();
-        const uint32_t kb = st_base + stage_of<C::kStages>(j) * C::kStageBytes;
-        #pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const int c = ks >> 2;
-          const uint64_t adesc = tc::smem_desc(q_base + c * (kRows * 128) + (ks & 3) * 32, 16,
-                                               1024, tc::kSwizzle128B);
-          const uint64_t bdesc = tc::smem_desc(kb + c * C::kChunkTileBytes + (ks & 3) * 32, 16,
-                                               1024, tc::kSwizzle128B);
-          tc::mma_ss(tmem + C::kTmemS + sb * BN, adesc, bdesc, idesc_qk, ks > 0 ? 1u : 0u);
+        if (!progressed && next_pv < next_qk) {
+          const int i = next_pv, pb = i & 1;
+          if (mbar_try_wait(&bars->p_full[pb], (i >> 1) & 1) &&
+              (KEQV || mbar_try_wait(&bars->v_full[stage_of<C::kVS>(i)], round_of<C::kVS>(i)))) {
+            tc::fence_after();
+            const uint32_t vb =
+                KEQV ? k_base + stage_of<C::kKStages>(i) * C::kKBytes +
+                           dh * C::kVChunks * C::kChunkTileBytes
+                     : v_base + stage_of<C::kVS>(i) * C::kVBytes;
+            const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
+            #pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              const uint64_t bdesc = tc::smem_desc(vb + ks * 16 * 128, C::kChunkTileBytes, 1024,
+                                                   tc::kSwizzle128B);
+              tc::mma_ts(tmem + C::kTmemO, p_hi + ks * 8, bdesc, idesc_pv,
+                         (i > 0 || ks > 0) ? 1u : 0u);
+              tc::mma_ts(tmem + C::kTmemO, p_hi + BN / 2 + ks * 8, bdesc, idesc_pv, 1u);
+            }
+            tc::commit(&bars->p_free[pb]);
+            // V (or, with k_eq_v, the whole K part) of this stage is free once PV ends
+            tc::commit(KEQV ? &bars->k_empty[stage_of<C::kKStages>(i)]
+                            : &bars->v_empty[stage_of<C::kVS>(i)]);
+            ++next_pv;
+            progressed = true;
+          }
         }
-        tc::commit(&bars->s_full[sb]);
-        if (!KEQV) tc::commit(&bars->k_empty[stage_of<C::kStages>(j)]);  // K read by QK
-        if (j > 0) ok = issue_pv(j - 1);
+        if (progressed) {
+          idle_since = clock64();
+        } else if (*abort_flag || clock64() - idle_since > kWaitLimitCycles) {
+          ok = false;
+        }
       }
-      if (ok && j == nkt && !*abort_flag) ok = issue_pv(nkt - 1);
       if (!ok) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
       // every MMA this thread issued has finished before tensor memory is freed
       tc::commit(&bars->mma_drained);
@@ -358,8 +408,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool use_cap = softcap > 0.f;
     const float inv_cap = use_cap ? 1.f / softcap : 0.f;
-    const float cap_l2 = softcap * kLog2e;
     const float scale_l2 = scale * kLog2e;
+    const float mul = use_cap ? softcap * kLog2e : 1.f;  // log2-domain value of the proxy
     float m_run = -INFINITY, l_run = 0.f;
     volatile int* sm_abort = &bars->sm_abort;
     const uint32_t pair_bar = 1 + quad;  // named barrier of warps quad and quad + 4
@@ -387,25 +437,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-        // scale (+ softcap) into the exp2 domain; every loop is branch-free
+        // scores to a monotone proxy u with log2-domain value mul * u: the tanh
+        // of the softcap (mul = cap log2 e) or the scaled score (mul = 1);
+        // every loop is branch-free
         if (use_cap) {
           const float sc = scale * inv_cap;
-          bool big = false;
+          const uint64_t sc2 = f2_pack(sc, sc);
+          float amax = 0.f;
           #pragma unroll
-          for (int k = 0; k < HALF; ++k) {
-            x[k] *= sc;
-            big |= fabsf(x[k]) > 0.5f;
+          for (int i = 0; i < HALF / 2; ++i) {
+            const float2 y = f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), sc2));
+            x[2 * i] = y.x;
+            x[2 * i + 1] = y.y;
+            amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
           }
-          if (__any_sync(0xffffffffu, big)) {
+          if (__any_sync(0xffffffffu, amax > 0.5f)) {
             #pragma unroll
-            for (int k = 0; k < HALF; ++k) x[k] = cap_l2 * tanh_any(x[k]);
+            for (int k = 0; k < HALF; ++k) x[k] = tanh_any(x[k]);
           } else {
             #pragma unroll
-            for (int k = 0; k < HALF; ++k) x[k] = cap_l2 * tanh_small(x[k]);
+            for (int i = 0; i < HALF / 2; ++i) {
+              const float2 t = f2_unpack(tanh_small2(f2_pack(x[2 * i], x[2 * i + 1])));
+              x[2 * i] = t.x;
+              x[2 * i + 1] = t.y;
+            }
           }
         } else {
+          const uint64_t s2 = f2_pack(scale_l2, scale_l2);
           #pragma unroll
-          for (int k = 0; k < HALF; ++k) x[k] *= scale_l2;
+          for (int i = 0; i < HALF / 2; ++i) {
+            const float2 t = f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), s2));
+            x[2 * i] = t.x;
+            x[2 * i + 1] = t.y;
+          }
         }
         // band + causal predicate only where the tile straddles this row's edges
         const bool interior = row_ok && key0 >= vis_lo && key0 + HALF - 1 <= p;
@@ -419,11 +483,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         #pragma unroll
         for (int k = 0; k < HALF; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
-        bars->red_max[sb][half][r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        bars->red[half][r] = mul * fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
       named_bar_sync(pair_bar, 64);  // the two halves of these rows meet
       if (okw) {
-        const float m_tile = fmaxf(bars->red_max[sb][0][r], bars->red_max[sb][1][r]);
+        const float m_tile = fmaxf(bars->red[0][r], bars->red[1][r]);
         if (m_tile > m_run + kRescaleThreshold) {  // lazy rescale (also the first visible key)
           alpha = ex2_approx(m_run - m_tile);
           m_run = m_tile;
@@ -452,13 +516,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         // zero V rows that no row of this tile can see (first / last key tile)
         if (j == 0 || j == nkt - 1) {
           const int tkey0 = (kt0 + j) * BN;
-          uint8_t* st = stages + stage_of<C::kStages>(j) * C::kStageBytes;
-          uint8_t* vt = KEQV ? st + dh * C::kVChunks * C::kChunkTileBytes : st + C::kKBytes;
+          uint8_t* vt = KEQV ? k_ring + stage_of<C::kKStages>(j) * C::kKBytes +
+                                   dh * C::kVChunks * C::kChunkTileBytes
+                             : v_ring + stage_of<C::kVS>(j) * C::kVBytes;
           const int z_lo = max(0, j_lo - tkey0);       // rows [0, z_lo) hidden
           const int z_hi = min(BN, j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
           if (!KEQV && (z_lo > 0 || z_hi < BN))  // V may land after K
-            okw = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[stage_of<C::kStages>(j)],
-                                                    round_of<C::kStages>(j)));
+            okw = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[stage_of<C::kVS>(j)],
+                                                    round_of<C::kVS>(j)));
           if (okw && (z_lo > 0 || z_hi < BN)) {
             for (int idx = threadIdx.x; idx < C::kVChunks * BN * 8; idx += kSoftmaxWarps * 32) {
               const int cv = idx / (BN * 8);
@@ -479,17 +544,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       if (okw) {
         // P = 2^(x - m): bf16 high part and bf16 remainder into tensor memory
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t mul2 = f2_pack(mul, mul), negm2 = f2_pack(-m_use, -m_use);
+        uint64_t ps2[2] = {0ull, 0ull};
         uint32_t hi[HALF / 2], lo[HALF / 2];
         #pragma unroll
         for (int i = 0; i < HALF / 2; ++i) {
-          const float a = ex2_approx(x[2 * i] - m_use);
-          const float bb = ex2_approx(x[2 * i + 1] - m_use);
-          ps[i & 3] += a + bb;
-          hi[i] = pack_bf16x2(a, bb);
-          const float2 hf = unpack_bf16x2(hi[i]);
-          lo[i] = pack_bf16x2(a - hf.x, bb - hf.y);
+          const float2 z = f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, negm2));
+          const float a = ex2_approx(z.x), bb = ex2_approx(z.y);
+          const uint64_t ab = f2_pack(a, bb);
+          ps2[i & 1] = f2_add(ps2[i & 1], ab);
+          // P = hi + lo without conversion instructions: hi keeps the upper 16
+          // bits of P (bf16 by truncation), lo = P - hi exactly, then truncated
+          // to bf16 the same way; together they carry P to 2^-14 relative.
+          const uint32_t ha = __float_as_uint(a) & 0xFFFF0000u;
+          const uint32_t hb = __float_as_uint(bb) & 0xFFFF0000u;
+          hi[i] = __byte_perm(ha, hb, 0x7632);
+          const float2 l = f2_unpack(f2_sub(ab, f2_pack(__uint_as_float(ha), __uint_as_float(hb))));
+          lo[i] = __byte_perm(__float_as_uint(l.x), __float_as_uint(l.y), 0x7632);
         }
+        const float2 ps_a = f2_unpack(ps2[0]), ps_b = f2_unpack(ps2[1]);
+        float ps[4] = {ps_a.x, ps_a.y, ps_b.x, ps_b.y};
         const uint32_t pcol = tmem + lane_off + C::kTmemP + sb * BN + half * (HALF / 2);
         if constexpr (HALF / 2 == 16) {
           tc::st16(pcol, hi);
@@ -512,14 +586,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     }
     bool ok = !*sm_abort;
 
-    // epilogue: l from both halves, O / l to global, lse
-    bars->red_sum[half][r] = l_run;
+    // epilogue: l from both halves, O / l to global, lse (the max exchange
+    // buffer is free: every softmax warp passed the last tile's barrier)
+    bars->red[half][r] = l_run;
     if (ok) ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars->p_free[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1));
     named_bar_sync(pair_bar, 64);
     tc::fence_after();
     if (ok) {
-      const float l_tot = bars->red_sum[0][r] + bars->red_sum[1][r];
+      const float l_tot = bars->red[0][r] + bars->red[1][r];
       const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
       float* orow = out + (static_cast<int64_t>(q0 + i0 + t) * n_q + kvh * group + h) * HD +
                     dh * C::kOCols + half * (C::kOCols / 2);
