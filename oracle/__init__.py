@@ -106,16 +106,21 @@ class Oracle:
                                                     head_dim, dtype_bytes, int(with_v)))
 
     def kv_cache_write(self, k_new, v_new, cu_new, past_lens, block_table, k_pool, v_pool,
-                       block_size: int = 16):
-        """Returns (k_pool', v_pool', status): copies of the pools with the new
-        rows written. ``v_pool`` None means V aliases the K pages."""
+                       block_size: int = 16, in_place: bool = False):
+        """Returns (k_pool', v_pool', status): the pools with the new rows
+        written (copies, or the given arrays themselves when ``in_place``).
+        ``v_pool`` None means V aliases the K pages."""
         k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
         cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
         past_lens = np.ascontiguousarray(past_lens, dtype=np.int32)
         block_table = np.ascontiguousarray(block_table, dtype=np.int32)
-        k_out = np.array(k_pool, dtype=np.uint16, copy=True, order="C")
-        v_out = None if v_pool is None else np.array(v_pool, dtype=np.uint16, copy=True,
-                                                     order="C")
+        if in_place:
+            assert k_pool.dtype == np.uint16 and k_pool.flags["C_CONTIGUOUS"]
+            k_out, v_out = k_pool, v_pool
+        else:
+            k_out = np.array(k_pool, dtype=np.uint16, copy=True, order="C")
+            v_out = None if v_pool is None else np.array(v_pool, dtype=np.uint16, copy=True,
+                                                         order="C")
         v_new_c = None if v_pool is None else np.ascontiguousarray(v_new, dtype=np.uint16)
         n_seqs = past_lens.shape[0]
         num_blocks, bs, n_kv, hd = k_out.shape

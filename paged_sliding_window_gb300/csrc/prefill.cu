@@ -586,29 +586,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     }
     bool ok = !*sm_abort;
 
-    // epilogue: l from both halves, O / l to global, lse (the max exchange
-    // buffer is free: every softmax warp passed the last tile's barrier)
+    // epilogue: l from both halves, O / l staged through shared memory (the Q
+    // tile and the K/V rings are idle once the last PV is done) and written out
+    // as whole rows with coalesced stores, lse
     bars->red[half][r] = l_run;
     if (ok) ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars->p_free[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1));
     named_bar_sync(pair_bar, 64);
     tc::fence_after();
+    const float l_tot = bars->red[0][r] + bars->red[1][r];
+    const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+    // staging rows of kOCols floats plus 16 bytes of padding: 32 lanes storing
+    // 16 bytes each at the same column of 32 rows then take the minimum four
+    // shared-memory wavefronts
+    constexpr int kORow = C::kOCols * 4 + 16;
+    static_assert(kRows * kORow <= C::kQBytes + C::kKStages * C::kKBytes +
+                                       C::kVStages * C::kVBytes,
+                  "O staging fits in the Q tile and the K/V rings");
+    uint8_t* ostage = q_smem;  // Q, then the K and V rings: contiguous and idle now
     if (ok) {
-      const float l_tot = bars->red[0][r] + bars->red[1][r];
-      const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-      float* orow = out + (static_cast<int64_t>(q0 + i0 + t) * n_q + kvh * group + h) * HD +
-                    dh * C::kOCols + half * (C::kOCols / 2);
       #pragma unroll 1
       for (int c16 = 0; c16 < C::kOCols / 32; ++c16) {
+        const int col0 = half * (C::kOCols / 2) + c16 * 16;
         uint32_t v[16];
-        tc::ld16(tmem + lane_off + C::kTmemO + half * (C::kOCols / 2) + c16 * 16, v);
+        tc::ld16(tmem + lane_off + C::kTmemO + col0, v);
         tc::wait_ld();
-        if (row_ok) {
-          #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(orow + c16 * 16 + i) =
-                make_float4(__uint_as_float(v[i]) * inv_l, __uint_as_float(v[i + 1]) * inv_l,
-                            __uint_as_float(v[i + 2]) * inv_l, __uint_as_float(v[i + 3]) * inv_l);
+        #pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float4 w;
+          w.x = __uint_as_float(v[4 * q4 + 0]) * inv_l;
+          w.y = __uint_as_float(v[4 * q4 + 1]) * inv_l;
+          w.z = __uint_as_float(v[4 * q4 + 2]) * inv_l;
+          w.w = __uint_as_float(v[4 * q4 + 3]) * inv_l;
+          *reinterpret_cast<float4*>(ostage + r * kORow + (col0 + 4 * q4) * 4) = w;
         }
       }
       if (row_ok && dh == 0 && half == 0 && lse != nullptr)
@@ -617,6 +627,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     } else if (lane == 0) {
       flag_error(err, PSW_DEVERR_PIPELINE);
       *abort_flag = 1;  // stops the producer and the MMA issuer
+    }
+    named_bar_sync(9, kSoftmaxWarps * 32);  // the whole O tile is staged
+    if (ok) {
+      // warp w copies rows w, w + 8, ...: 32 lanes x 16 bytes per store
+      const int rows_valid = min(group * T, tok_valid * group);
+      for (int rr = warp; rr < rows_valid; rr += kSoftmaxWarps) {
+        const int tt = rr / group, hh = rr - tt * group;
+        float* orow = out + (static_cast<int64_t>(q0 + i0 + tt) * n_q + kvh * group + hh) * HD +
+                      dh * C::kOCols;
+        #pragma unroll
+        for (int c = lane; c < C::kOCols / 4; c += 32)
+          reinterpret_cast<float4*>(orow)[c] =
+              *reinterpret_cast<const float4*>(ostage + rr * kORow + c * 16);
+      }
     }
   }
 

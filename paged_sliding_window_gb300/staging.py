@@ -69,3 +69,40 @@ class GpuStep:
         binding.attn_prefill_chunked(self.step.layer, self.q, self.cu_new, self.past, max_q,
                                      self.k_pool, self.v_pool, self.pages, self.out, self.lse,
                                      self.ws)
+
+
+class MixedLayerStep:
+    """One layer of a mixed serving step on the GPU: the first ``n_decode``
+    sequences decode one token each, the rest prefill a chunk. One cache write
+    covers every new token; decode and prefill then run on their own rows of
+    the shared block table."""
+
+    def __init__(self, step: wl.Step, n_decode: int, device="cuda"):
+        self.g = GpuStep(step, device)
+        self.step, self.n_decode = step, n_decode
+        g = self.g
+        nd = n_decode
+        self.dec_q = g.q[:nd]
+        self.dec_lens = g.seq_lens[:nd]
+        self.dec_out = g.out[:nd]
+        self.dec_lse = g.lse[:nd]
+        self.dec_table = g.table[:nd]
+        self.dec_pages = binding.make_pages(self.dec_table, step.cache.num_blocks)
+        row0 = int(step.cu_new[nd])
+        self.pre_q = g.q[row0:]
+        self.pre_cu = (g.cu_new[nd:] - row0).contiguous()
+        self.pre_past = g.past[nd:].contiguous()
+        self.pre_out = g.out[row0:]
+        self.pre_lse = g.lse[row0:]
+        self.pre_table = g.table[nd:].contiguous()
+        self.pre_pages = binding.make_pages(self.pre_table, step.cache.num_blocks)
+        self.max_chunk = int(step.new_lens[nd:].max()) if step.n_seqs > nd else 0
+
+    def run(self):
+        g, L = self.g, self.step.layer
+        g.write_new()
+        binding.attn_decode_paged(L, self.dec_q, g.k_pool, g.v_pool, self.dec_pages,
+                                  self.dec_lens, self.dec_out, self.dec_lse, g.ws)
+        binding.attn_prefill_chunked(L, self.pre_q, self.pre_cu, self.pre_past, self.max_chunk,
+                                     g.k_pool, g.v_pool, self.pre_pages, self.pre_out,
+                                     self.pre_lse, g.ws)
