@@ -41,9 +41,11 @@ from paged_sliding_window_gb300 import workloads as wl  # noqa: E402
 METRIC = "decode attn KV-read GB/s (% of HBM peak)"
 UNIT = "GB/s"
 WORKLOAD = "sliding-layer decode batch"
-PROFILE = os.path.join(ROOT, "profiles", "decode_split_sliding_decode_batch.md")
-KERNEL_SOURCES = [os.path.join(ROOT, "paged_sliding_window_gb300", "csrc", f)
-                  for f in ("decode.cu", "ptx.cuh")]
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "paged_sliding_window_gb300", "csrc")
+# ncu summary per measured kernel, and the sources whose hash it was taken at.
+PROFILE_DECODE = ("decode_split_sliding_decode_batch.md", ("decode.cu", "ptx.cuh"))
+PROFILE_PREFILL = ("prefill_chunked_prefill_softcap.md", ("prefill.cu", "ptx.cuh"))
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -86,23 +88,24 @@ def prefill_flops(step: wl.Step) -> int:
     return 4 * L.head_dim * L.n_q_heads * total
 
 
-def source_sha() -> str:
+def source_sha(files=PROFILE_DECODE[1]) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(p, "rb") as f:
-            h.update(f.read())
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since it was captured."""
-    if not os.path.exists(PROFILE):
+def profiled_traffic(profile=PROFILE_DECODE):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of
+    that kernel, or None when its sources changed since it was captured."""
+    path = os.path.join(PROFILES, profile[0])
+    if not os.path.exists(path):
         return None
-    text = open(PROFILE).read()
+    text = open(path).read()
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     m_s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_b or not m_s or m_s.group(1) != source_sha():
+    if not m_b or not m_s or m_s.group(1) != source_sha(profile[1]):
         return None
     return float(m_b.group(1))
 
@@ -239,6 +242,22 @@ def config_of(step: wl.Step) -> dict:
             "parallelism": "replicas"}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of per-rank timings (the job's time is its slowest
+    replica's); identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units of all replicas divided by the slowest replica's time (weak scaling)."""
+    return units_per_rank * world / seconds
+
+
 def flush_l2(buf):
     buf.add_(1)
 
@@ -287,7 +306,7 @@ def measure_prefill(steps, warmup, tflops_peak, peak_kind):
             "roofline": {"bound": "tensor", "kernel": "prefill_kernel<256, false>",
                          "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
                          "frac": achieved / tflops_peak, "peak_kind": peak_kind + " bf16 burst",
-                         "traffic": None},
+                         "traffic": profiled_traffic(PROFILE_PREFILL)},
             "gpu_launches_per_call": 1}
 
 
@@ -312,6 +331,72 @@ def measure_full_decode(steps, warmup, hbm, peak_kind):
             "roofline": {"bound": "hbm", "kernel": "attn_decode_paged (plan + split + merge)",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None}}
+
+
+def decode_kv_bytes_subset(step: wl.Step, n: int) -> int:
+    L = step.layer
+    lens = step.seq_lens[:n].astype(np.int64)
+    keys = np.minimum(lens, L.window) if L.window > 0 else lens
+    return int(keys.sum()) * L.n_kv_heads * L.head_dim * 2 * (1 if L.k_eq_v else 2)
+
+
+def prefill_flops_subset(step: wl.Step, first: int) -> int:
+    L = step.layer
+    total = 0
+    for b in range(first, step.n_seqs):
+        n = int(step.new_lens[b])
+        pos = int(step.past_lens[b]) + np.arange(n, dtype=np.int64)
+        vis = np.minimum(pos + 1, L.window) if L.window > 0 else pos + 1
+        total += int(vis.sum())
+    return 4 * L.head_dim * L.n_q_heads * total
+
+
+def measure_mixed(steps, warmup):
+    """Mixed serving step over the 6-layer hybrid stack: per layer one cache
+    write, decode of 256 sequences and prefill of 4 chunks of 2048 tokens."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+    from paged_sliding_window_gb300.staging import MixedLayerStep
+    work = wl.mixed_hybrid(threads=16)
+    nd = work.decode_seqs
+    layers = [MixedLayerStep(s, nd) for s in work.steps]
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for m in layers:
+            m.run()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        row = []
+        for m in layers:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            L = m.step.layer
+            g = m.g
+            e[0].record(stream)
+            g.write_new()
+            e[1].record(stream)
+            binding.attn_decode_paged(L, m.dec_q, g.k_pool, g.v_pool, m.dec_pages, m.dec_lens,
+                                      m.dec_out, m.dec_lse, g.ws)
+            e[2].record(stream)
+            binding.attn_prefill_chunked(L, m.pre_q, m.pre_cu, m.pre_past, m.max_chunk, g.k_pool,
+                                         g.v_pool, m.pre_pages, m.pre_out, m.pre_lse, g.ws)
+            e[3].record(stream)
+            row.append(e)
+        evs.append(row)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    t_write = statistics.mean(sum(r[i][0].elapsed_time(r[i][1]) for i in range(6)) for r in evs)
+    t_dec = statistics.mean(sum(r[i][1].elapsed_time(r[i][2]) for i in range(6)) for r in evs)
+    t_pre = statistics.mean(sum(r[i][2].elapsed_time(r[i][3]) for i in range(6)) for r in evs)
+    t_step = statistics.mean(r[0][0].elapsed_time(r[5][3]) for r in evs)
+    dec_bytes = sum(decode_kv_bytes_subset(m.step, nd) for m in layers)
+    pre_flops = sum(prefill_flops_subset(m.step, nd) for m in layers)
+    return {"workload": "mixed hybrid step (6 layers, 256 decode + 4 x 2048 prefill)",
+            "ms_per_step": t_step, "kv_cache_write_ms": t_write, "decode_ms": t_dec,
+            "prefill_ms": t_pre, "decode_kv_bytes": dec_bytes,
+            "decode_GBps": dec_bytes / (t_dec / 1e3) / 1e9, "prefill_flops": pre_flops,
+            "prefill_TFLOPs": pre_flops / (t_pre / 1e3) / 1e12,
+            "gpu_launches_per_step": 6 * (1 + 2 + 1)}
 
 
 def ncu_case(which):
@@ -349,7 +434,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the prefill and full-layer decode measurements")
+                    help="skip the prefill, full-layer decode and mixed-step measurements")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
     ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None)
     args = ap.parse_args()
     if args.ncu_case:
@@ -463,13 +549,10 @@ def main():
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     assert binding.get_error() == 0, "device error flagged during the timed steps"
 
-    times = torch.tensor([elapsed_ms, e2e_s], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms, e2e_s = float(times[0]), float(times[1])
+    elapsed_ms, e2e_s = max_over_ranks([elapsed_ms, e2e_s], dist, "cuda")
     ms_per_step = elapsed_ms / args.steps
-    value = nbytes * world / (ms_per_step / 1e3) / 1e9
-    e2e_value = nbytes * world / e2e_s / 1e9
+    value = whole_job_rate(nbytes, world, ms_per_step / 1e3) / 1e9
+    e2e_value = whole_job_rate(nbytes, world, e2e_s) / 1e9
 
     hbm, _, peak_kind = peaks()
     achieved = (nbytes + io_bytes(step)) / (decode_ms / 1e3) / 1e9
@@ -492,6 +575,8 @@ def main():
         hbm_p, tf_p, kind_p = peaks()
         line["prefill"] = measure_prefill(args.steps, args.warmup, tf_p, kind_p)
         line["full_keqv_decode"] = measure_full_decode(args.steps, args.warmup, hbm_p, kind_p)
+        if not args.no_mixed:
+            line["mixed_hybrid_step"] = measure_mixed(min(args.steps, 10), 3)
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
