@@ -47,6 +47,18 @@ CSRC = os.path.join(ROOT, "paged_sliding_window_gb300", "csrc")
 PROFILE_DECODE = ("decode_split_sliding_decode_batch.md", ("decode.cu", "ptx.cuh"))
 PROFILE_PREFILL = ("prefill_chunked_prefill_softcap.md", ("prefill.cu", "ptx.cuh"))
 L2_BYTES = 129 * 1024 * 1024
+# kv_cache_write_kernel, decode_plan_kernel, decode_split_kernel
+LAUNCHES_PER_STEP = 3
+
+
+_WORKLOADS = {}
+
+
+def first_step(name: str) -> wl.Step:
+    """First step of a named workload, generated once per process."""
+    if name not in _WORKLOADS:
+        _WORKLOADS[name] = getattr(wl, name)().steps[0]
+    return _WORKLOADS[name]
 
 
 def peaks():
@@ -89,10 +101,15 @@ def prefill_flops(step: wl.Step) -> int:
 
 
 def source_sha(files=PROFILE_DECODE[1]) -> str:
+    """Hash of the kernel sources without whole-line comments and blank lines,
+    so that a comment edit does not void a profile of unchanged code."""
     h = hashlib.sha256()
     for f in files:
         with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+            for line in fh.read().splitlines():
+                t = line.strip()
+                if t and not t.startswith(b"//"):
+                    h.update(line + b"\n")
     return h.hexdigest()[:16]
 
 
@@ -164,17 +181,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None):
+def oracle_pools(orc, step: wl.Step):
+    c = step.cache
+    kp, vp = c.empty_pools()
+    orc.kv_cache_write(c.hist_k, c.hist_v, c.hist_cu, c.hist_past, step.block_table, kp, vp,
+                       in_place=True)
+    orc.kv_cache_write(step.new_k, step.new_v, step.cu_new, step.past_lens, step.block_table,
+                       kp, vp, in_place=True)
+    return kp, vp
+
+
+def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None, threads=0, pools=None):
     """Times the fp64 oracle on (a subset of) the step; returns
     (GB/s, threads, description)."""
     import oracle
     orc = oracle.default()
-    c = step.cache
-    k0, v0 = c.empty_pools()
-    k1, v1, _ = orc.kv_cache_write(c.hist_k, c.hist_v, c.hist_cu, c.hist_past, step.block_table,
-                                   k0, v0)
-    kp, vp, _ = orc.kv_cache_write(step.new_k, step.new_v, step.cu_new, step.past_lens,
-                                   step.block_table, k1, v1)
+    kp, vp = oracle_pools(orc, step) if pools is None else pools
     idx = np.arange(step.n_seqs) if seqs is None else np.asarray(seqs)
     L = step.layer
     lens = step.seq_lens[idx].astype(np.int64)
@@ -183,14 +205,50 @@ def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None):
     passes, t_total, threads = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
         t0 = time.perf_counter()
-        _, _, threads = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table, step.seq_lens,
-                                   seqs=idx)
+        _, _, used = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table, step.seq_lens,
+                                seqs=idx, threads=threads)
         t_total += time.perf_counter() - t0
         passes += 1
     gbs = nbytes * passes / t_total / 1e9
     desc = (f"fp64 C oracle, {len(idx)} of {step.n_seqs} sequences x all heads, "
             f"{passes} passes in {t_total:.1f} s")
-    return gbs, threads, desc
+    return gbs, used, desc
+
+
+def cpu_oracle_prefill(step: wl.Step, budget_s: float, every: int = 64):
+    """Times the fp64 oracle on every `every`-th chunk row of a prefill step;
+    returns (TFLOP/s counting visible pairs, threads, description)."""
+    import oracle
+    orc = oracle.default()
+    kp, vp = oracle_pools(orc, step)
+    L = step.layer
+    rows = np.arange(0, int(step.cu_new[-1]), every, dtype=np.int64)
+    seq_of = np.searchsorted(step.cu_new, rows, side="right") - 1
+    pos = step.past_lens[seq_of].astype(np.int64) + rows - step.cu_new[seq_of]
+    vis = np.minimum(pos + 1, L.window) if L.window > 0 else pos + 1
+    flops = 4 * L.head_dim * L.n_q_heads * int(vis.sum())
+    passes, t_total, used = 0, 0.0, 0
+    while passes == 0 or t_total < budget_s:
+        t0 = time.perf_counter()
+        _, _, used = orc.prefill(L.as_dict(), step.q, step.cu_new, step.past_lens, kp, vp,
+                                 step.block_table, rows=rows)
+        t_total += time.perf_counter() - t0
+        passes += 1
+    rate = flops * passes / t_total / 1e12
+    desc = (f"fp64 C oracle, every {every}th of {int(step.cu_new[-1])} chunk rows x all heads, "
+            f"{passes} passes in {t_total:.1f} s")
+    return rate, used, desc
+
+
+def cpu_oracle_extra(budget_s: float) -> dict:
+    """Oracle rates on the host cores for the other workloads (bounded samples)."""
+    step = first_step("full_keqv_decode")
+    gbs, cores, desc = cpu_oracle_gbs(step, budget_s, seqs=np.arange(0, step.n_seqs, 4))
+    out = {"full_keqv_decode": {"value": gbs, "unit": "GB/s", "cores": cores, "sample": desc}}
+    step = first_step("chunked_prefill")
+    tf, cores, desc = cpu_oracle_prefill(step, budget_s)
+    out["prefill"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "sample": desc}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -288,7 +346,7 @@ def measure_prefill(steps, warmup, tflops_peak, peak_kind):
     import torch
     from paged_sliding_window_gb300 import binding
     from paged_sliding_window_gb300.staging import GpuStep
-    step = wl.chunked_prefill().steps[0]
+    step = first_step("chunked_prefill")
     g = GpuStep(step)
     flops = prefill_flops(step)
     scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
@@ -315,7 +373,7 @@ def measure_full_decode(steps, warmup, hbm, peak_kind):
     import torch
     from paged_sliding_window_gb300 import binding
     from paged_sliding_window_gb300.staging import GpuStep
-    step = wl.full_keqv_decode().steps[0]
+    step = first_step("full_keqv_decode")
     g = GpuStep(step)
     g.write_new()
     nbytes = kv_bytes(step)
@@ -417,7 +475,7 @@ def ncu_case(which):
         for _ in range(3):
             g.decode()
     else:
-        step = wl.chunked_prefill().steps[0]
+        step = first_step("chunked_prefill")
         g = GpuStep(step)
         g.write_new()
         for _ in range(3):
@@ -567,7 +625,7 @@ def main():
                      "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": traffic},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "stage_ms": {"kv_cache_write": write_ms, "attn_decode_paged": decode_ms},
         "clocks": clock_info,
     }
@@ -578,9 +636,18 @@ def main():
         if not args.no_mixed:
             line["mixed_hybrid_step"] = measure_mixed(min(args.steps, 10), 3)
     if rank == 0 and world == 1 and args.cpu_budget > 0:
-        gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget)
+        import oracle
+        pools = oracle_pools(oracle.default(), step)
+        gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget, pools=pools)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc}
+        gbs1, _, desc1 = cpu_oracle_gbs(step, args.cpu_budget / 4, seqs=np.arange(0, 64, 8),
+                                        threads=1, pools=pools)
+        line["cpu_baseline"]["single_core"] = {"value": gbs1, "unit": UNIT, "cores": 1,
+                                               "sample": desc1}
+        del pools
+        if not args.no_extra:
+            line["cpu_baseline"]["other_workloads"] = cpu_oracle_extra(args.cpu_budget / 3)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -29,8 +29,11 @@
 //  * A unit whose tiles all fall in one CTA writes its normalised output
 //    directly; units cut by a slice boundary leave (m, l, O) partials in the
 //    workspace (slot = CTA + unit, which is unique because slices and units
-//    are both contiguous in tile order) and a merge kernel combines them with
-//    the log-sum-exp rule.
+//    are both contiguous in tile order). Each such CTA then takes a ticket on
+//    the unit; the one that takes the last ticket combines all partials with
+//    the log-sum-exp rule. No CTA ever waits for another.
+//  * While a unit's last tile is in flight, the consumers load the next
+//    unit's queries into registers.
 //  * Rows of a partially visible page (before the window start or past the
 //    end) are masked in the scores and their V rows zeroed in shared memory,
 //    so stale or non-finite cache contents never reach the output.
