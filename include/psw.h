@@ -172,10 +172,14 @@ PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const voi
  *   max_q_len  host bound on every chunk length (cu_q[b+1] - cu_q[b]); longer
  *              chunks are flagged (PSW_DEVERR_LENGTH) and their excess rows skipped
  *   out        device fp32 [n_q_total][n_q_heads][head_dim]; lse fp32 [n_q_total][n_q_heads] or NULL
- *   ws, ws_bytes  unused by this kernel (may be NULL / 0)
+ *   ws         device workspace of ws_bytes >= psw_workspace_bytes(layer, n_seqs, L)
+ *              for any L >= max_q_len; it holds the work list of the call
  * Tensor-core kernel (tcgen05 MMAs with S, P and O in tensor memory, K/V tiles
  * fed by TMA through the block table); key tiles that the band rule hides from
- * every row of a query tile are never loaded. Needs n_q_heads / n_kv_heads <= 128.
+ * every row of a query tile are never loaded. A small plan kernel first orders
+ * the work (blocks of 128 / G chunk tokens per KV head) longest first; a
+ * persistent grid then takes it in that order. Needs n_q_heads / n_kv_heads
+ * <= 128 and n_seqs <= 65535; PSW_EWORKSPACE when ws is missing or too small.
  */
 PSW_API int attn_prefill_chunked(const psw_layer_t *layer, const void *q, const int32_t *cu_q,
                          const int32_t *past_lens, int32_t n_seqs, int32_t n_q_total,

@@ -148,6 +148,26 @@ int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks,
   return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
 }
 
+int make_pool_page_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv, int hd,
+                       int box_chunks) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return PSW_ETENSORMAP;
+  // [chunk of 64 elements across (kv head, head_dim)][slot][64 elements]: one
+  // box is a whole page (16 slots) of box_chunks chunks and lands in shared
+  // memory as [chunk][16 rows][128 B]
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * kBlockSize,
+                              static_cast<cuuint64_t>(n_kv) * (hd / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n_kv) * hd * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
+                             static_cast<cuuint32_t>(box_chunks)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
+}
+
 int make_query_tensor_map(CUtensorMap* map, const void* q, int n_q_total, int n_q, int hd,
                           int group) {
   EncodeTiledFn enc = encode_fn();
@@ -180,7 +200,9 @@ int psw_workspace_bytes(const psw_layer_t* layer, int32_t n_seqs, int32_t max_se
   if (bytes == nullptr) return PSW_ENULL;
   if (n_seqs < 0) return PSW_EINVAL_NSEQS;
   if (max_seq_len < 0) return PSW_ECAPACITY;
-  *bytes = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total;
+  const size_t dec = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total;
+  const size_t pre = prefill_workspace_bytes(L, n_seqs, max_seq_len);
+  *bytes = dec > pre ? dec : pre;
   return PSW_OK;
 }
 
@@ -259,10 +281,15 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
   if (max_q_len < 0 || n_q_total < 0) return PSW_ECAPACITY;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PSW_EALIGN;
-  (void)ws;
-  (void)ws_bytes;
   if (n_seqs == 0 || max_q_len == 0 || n_q_total == 0) return PSW_OK;
   if (n_seqs > 65535) return PSW_EINVAL_NSEQS;
+  // work items (sequence, block of 128 / G tokens, KV head, head_dim half) must
+  // be countable in 32 bits
+  const int64_t blocks = (static_cast<int64_t>(max_q_len) + 128 / L.group() - 1) / (128 / L.group());
+  if (static_cast<int64_t>(n_seqs) * blocks * L.n_kv * (L.hd / 256) > 0x7fffffffLL)
+    return PSW_ECAPACITY;
+  if (ws == nullptr || ws_bytes < prefill_workspace_bytes(L, n_seqs, max_q_len))
+    return PSW_EWORKSPACE;
   DeviceState* st;
   if ((rc = device_ready(&st)) != PSW_OK) return rc;
   CUtensorMap q_map, k_map, v_map;
@@ -272,13 +299,14 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
     return rc;
   if (L.k_eq_v) {
     v_map = k_map;
-  } else if ((rc = make_pool_tensor_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd)) !=
+  } else if ((rc = make_pool_page_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd, 4)) !=
              PSW_OK) {
     return rc;
   }
   return launch_prefill(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs, n_q_total, max_q_len,
                         pages->block_table, pages->max_blocks_per_seq, pages->num_blocks, out,
-                        lse, st->err, reinterpret_cast<cudaStream_t>(stream));
+                        lse, ws, st->info.num_sms, st->err,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 int psw_get_error(psw_stream_t stream, int32_t* device_error_out) {

@@ -12,37 +12,45 @@
 // ("Gemma 4 model architecture analysis", sections 6.3 and 6.5); the key range
 // of a tile is cut to what the band leaves visible (the PR's follow-up item 2).
 //
-// Design (how, on sm_103a), one CTA per (sequence, KV head, block of 128/G
-// chunk tokens, half of head_dim for head_dim 512):
-//  * 128 query rows = (128/G tokens) x (G heads), token-major. Q is loaded once
-//    by TMA (128-byte swizzle, one box per 64 columns of head_dim).
-//  * Warps 8 (Q, K) and 10 (V) stream K and V tiles of BN keys (64 for
-//    head_dim 256, 32 for 512) into rings of their own (3 K and 2 V stages
-//    where shared memory allows), one 2 KB TMA box per (page, 64-column
-//    chunk), and warm L2 with the tile three ahead. A K stage is released as
-//    soon as QK has read it, a V stage after PV. Pages past the sequence end
-//    load as zeros.
-//  * Warp 9 (one elected thread) issues tcgen05.mma: S_j = Q K_j^T (SS, both
-//    K-major) into one of two S buffers in TMEM, and O += P_j V_j (TS: P from
-//    one of two P buffers in TMEM, V MN-major from shared memory). The issue
-//    order QK_0, QK_1, PV_0, QK_2, PV_1, ... keeps the tensor pipe fed while
-//    the softmax warps work on the tile before.
-//  * Warps 0-7 run the softmax. Warps w and w+4 own the same 32 rows (TMEM
-//    lanes 32 (w mod 4) ...) and split the BN key columns in halves; per tile
-//    they exchange one partial row maximum through shared memory. Scores get
-//    scale, softcap (odd polynomial on the FMA pipe for |s/cap| <= 1/2, the
-//    exp formula beyond) and, on band-edge tiles only, the band/causal
-//    predicate; the online softmax runs in fp32 in the exp2 domain with lazy
-//    rescaling of O (only when the running max grows by more than 2^8; the
-//    two warps of a row pair rescale half of O each). P is written back to
-//    TMEM as a bf16 high part and a bf16 remainder, split with integer ops
-//    (no conversion instructions); both are multiplied into O, so P enters the
-//    product to 2^-14 relative.
-//  * V rows of key positions that no row of the tile can see (before the
-//    window of the tile's first row, after its last row) are zeroed in shared
-//    memory so uncached or stale slots never reach O.
+// Design (how, on sm_103a):
+//  * Work item = (sequence, block of 128/G chunk tokens, KV head, half of
+//    head_dim for head_dim 512): 128 query rows = (128/G tokens) x (G heads),
+//    token-major. A plan kernel lists the (sequence, block) units sorted by
+//    their number of key tiles, longest first; a persistent grid of one CTA
+//    per SM takes items from that list with an atomic counter, so long items
+//    start first and short ones fill the gaps (longest-processing-time order).
+//  * Each CTA runs warp-specialised pipelines that carry on across items:
+//    warp 8 takes the next item, loads Q (TMA, 128-byte swizzle) and streams
+//    K tiles of BN keys (64 at head_dim 256, 32 at 512) into a ring; warp 10
+//    streams V tiles into a second ring; both warm L2 three tiles ahead. A K
+//    stage is released once QK has read it, a V stage after PV.
+//  * Two warps issue tcgen05.mma (one elected thread each): warp 9 the QK
+//    stream S_j = Q K_j^T (SS, both K-major) into one of two S buffers in
+//    tensor memory, warp 11 the PV stream O += P_j V_j (TS: P from one of two
+//    P buffers in tensor memory, V MN-major). QK of tile g + 2 runs while the
+//    softmax works on tile g; the next item's QK starts as soon as its Q has
+//    landed, while the softmax warps still finish the previous item.
+//  * Warps 0-3 run the softmax: warp w owns the 32 rows of tensor-memory lane
+//    quadrant w and all key columns of a tile, so row maxima and sums stay in
+//    one thread and the softmax warps never wait for each other. The row
+//    maximum comes from the raw scores (the softcap is monotone); the softcap
+//    is an odd polynomial on the FMA pipe where every |s/cap| of the warp's
+//    tile is at most 1/2 (the exp formula elsewhere); the band/causal
+//    predicate is applied on edge tiles only; the online softmax runs in fp32
+//    in the exp2 domain with lazy rescaling of O (only when the running
+//    maximum grows by more than 2^8). P is written back to tensor memory as a
+//    bf16 high part and a bf16 remainder (integer ops, no conversions); both
+//    are multiplied into O, so P enters the product to 2^-14 relative.
+//  * Warps 4-7 are the epilogue: once an item's last PV is done they scale
+//    its O by 1/l, stage it per warp through shared memory 32 columns at a
+//    time and write whole 128-byte row segments, while the softmax warps
+//    already work on the next item.
+//  * V rows of key positions that no row of the item can see (before the
+//    window of its first row, after its last row) are zeroed in shared memory
+//    so uncached or stale slots never reach O.
 //  * Every wait is bounded; on timeout the kernel flags PSW_DEVERR_PIPELINE,
-//    drains its own copies and MMAs, frees its tensor memory and returns.
+//    every role leaves its loop, drains its own copies and MMAs, and the
+//    tensor memory is freed before the CTA exits.
 #include <math.h>
 
 #include "psw_internal.h"
@@ -51,22 +59,33 @@
 namespace psw {
 namespace pf {
 
-constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8;   // Q and K tiles
-constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10; // V tiles (idle with k_eq_v)
-constexpr int kThreads = 11 * 32;
+constexpr int kSoftmaxWarps = 4;  // warps 0-3
+constexpr int kEpiWarps = 4;      // warps 4-7
+constexpr int kKWarp = 8;    // takes work items, loads Q and K tiles
+constexpr int kQkWarp = 9;   // tcgen05.mma issuer of the QK stream
+constexpr int kVWarp = 10;   // V tiles (idle with k_eq_v)
+constexpr int kPvWarp = 11;  // tcgen05.mma issuer of the PV stream
+constexpr int kThreads = 12 * 32;
 constexpr int kRows = 128;
 constexpr int kPageBoxBytes = kBlockSize * 128;  // one TMA box: 16 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
+constexpr int kCostBuckets = 4096;       // plan: units sorted by tile count (capped)
+constexpr int kPlanThreads = 1024;
+
+// Work list at the start of the workspace: this header, then int2 units.
+struct PlanHeader {
+  int32_t next_item;  // atomic work counter
+  int32_t n_units;    // (sequence, block) units in the list
+  int32_t pad[14];
+};
+static_assert(sizeof(PlanHeader) == 64, "plan header");
 
 template <int HD, bool KEQV>
 struct Cfg {
   static constexpr int kQChunks = HD / 64;
   static constexpr int kBN = (HD == 256) ? 64 : 32;
-  static constexpr int kHalf = kBN / 2;  // key columns per softmax warp
   static constexpr int kPagesPerTile = kBN / kBlockSize;
   static constexpr int kOCols = 256;
   static constexpr int kDSplit = HD / kOCols;
@@ -75,49 +94,217 @@ struct Cfg {
   static constexpr int kChunkTileBytes = kBN * 128;  // one 64-column chunk of a K/V tile
   static constexpr int kKBytes = kQChunks * kChunkTileBytes;
   static constexpr int kVBytes = KEQV ? 0 : kVChunks * kChunkTileBytes;
-  static constexpr int kBarsBytes = 1536;
-  static constexpr int kBudget = 232448 - 1024 - kQBytes - kBarsBytes;
-  // K and V have rings of their own: K is consumed early (QK), V late (PV).
-  // Three K stages where they fit (two for head_dim 512 without k_eq_v), two
-  // V stages (one when only that fits).
-  static constexpr int kKStages = (3 * kKBytes + 2 * kVBytes <= kBudget) ? 3 : 2;
-  static constexpr int kVStages = KEQV ? 0 : ((kKStages * kKBytes + 2 * kVBytes <= kBudget) ? 2 : 1);
-  static constexpr int kSmemBytes =
-      1024 + kQBytes + kKStages * kKBytes + kVStages * kVBytes + kBarsBytes;
+  static constexpr int kVPageBytes = kVChunks * kPageBoxBytes;  // one page of V
+  static constexpr int kBarsBytes = 2432;
+  static constexpr int kAvail = 232448 - kBarsBytes;
+  static constexpr int kRingBudget = kAvail - kQBytes;
+  static constexpr int kVStages = KEQV ? 0 : 2;
+  static constexpr int kKStagesFit = (kRingBudget - kVStages * kVBytes) / kKBytes;
+  static constexpr int kKStages = kKStagesFit > 4 ? 4 : kKStagesFit;
   static constexpr int kVS = kVStages > 0 ? kVStages : 1;  // ring size for index math
+  static constexpr int kUsed =
+      kQBytes + kKStages * kKBytes + kVStages * kVBytes + kBarsBytes;
+  // slack to round the dynamic shared memory base up to 1024 bytes (128-byte
+  // swizzle atoms); checked at run time
+  static constexpr int kSlack = (232448 - kUsed) < 1024 ? (232448 - kUsed) : 1024;
+  static constexpr int kSmemBytes = kUsed + kSlack;
   // tensor memory columns: O | S0 | S1 | P0 (hi, lo) | P1 (hi, lo)
   static constexpr int kTmemO = 0;
-  static constexpr int kTmemS = 256;                 // + b * kBN
-  static constexpr int kTmemP = 256 + 2 * kBN;       // + b * kBN; hi then lo (kBN/2 each)
+  static constexpr int kTmemS = 256;            // + b * kBN
+  static constexpr int kTmemP = 256 + 2 * kBN;  // + b * kBN; hi then lo (kBN/2 each)
   static constexpr int kTmemCols = 512;
-  static constexpr int kTmaPerStage = kPagesPerTile * (kQChunks + (KEQV ? 0 : kVChunks));
-  static_assert(kTmaPerStage <= 32, "one TMA box per producer lane");
+  static_assert(kKStages >= 2, "two K stages at least");
+  static_assert(kPagesPerTile * kQChunks <= 32 && kPagesPerTile * kVChunks <= 32,
+                "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kTmemP + 2 * kBN <= kTmemCols, "tensor memory columns");
-  static_assert(kKStages * kKBytes + kVStages * kVBytes <= kBudget, "K/V rings");
 };
-
-template <int S>
-__device__ __forceinline__ int stage_of(int j) { return j % S; }
-template <int S>
-__device__ __forceinline__ uint32_t round_of(int j) { return static_cast<uint32_t>(j / S) & 1u; }
 
 struct Bars {
-  uint64_t q_full;
-  // K and V rings are filled and released separately: a K stage is free once
-  // QK has read it, a V stage once PV has (with k_eq_v, V is the K stage and
-  // it is released after PV). First kKStages / kVStages entries used.
-  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full, o_free;
   uint64_t mma_drained;
+  int32_t item[2];
   uint32_t tmem_base;
-  int abort;     // set by any warp; read by the producer and the MMA issuer
-  int sm_abort;  // set only by softmax threads, read after their named barrier
-  float red[2][kRows];  // [column half][row]: partial row max per tile, then row sums
+  int32_t abort;
+  uint64_t stats_full[2], stats_free[2];  // row maxima and sums, per item parity
+  float stat_m[2][kRows], stat_l[2][kRows];
 };
 
-// tanh(y) for |y| <= 1/2: odd Taylor polynomial through y^11 (the next term
-// is below 4.4e-7). Branch-free, FMA pipe only.
+// Geometry of one (sequence, block) unit; uniform across a CTA.
+struct Geom {
+  int b, q0, past, i0, tok_valid;
+  int j_lo, j_hi;  // keys [j_lo, j_hi] are visible to some row of the block
+  int kt0, nkt;    // key tiles kt0 .. kt0 + nkt - 1
+  int last_page;   // last page index that may be read
+};
+
+// Returns false when the block has no rows. With `err`, length and capacity
+// problems are reported (once per sequence: by its first block).
+__device__ __forceinline__ bool unit_geom(int b, int rb, const int32_t* __restrict__ cu_q,
+                                          const int32_t* __restrict__ past_lens, int n_q_total,
+                                          int max_q_len, int max_blocks, int window, int T, int BN,
+                                          Geom& g, int32_t* err) {
+  const int q0 = cu_q[b];
+  int n_b = cu_q[b + 1] - q0;
+  const int past = past_lens[b];
+  // positions must stay far from int overflow (past + rows + one tile)
+  if (n_b < 0 || past < 0 || q0 < 0 ||
+      static_cast<int64_t>(past) + max_q_len > 0x7fffffffLL - 4096) {
+    if (err != nullptr && rb == 0) flag_error(err, PSW_DEVERR_LENGTH);
+    return false;
+  }
+  if (n_b > max_q_len || static_cast<int64_t>(q0) + n_b > n_q_total) {
+    if (err != nullptr && rb == 0) flag_error(err, PSW_DEVERR_LENGTH);
+    n_b = min(max_q_len, n_q_total - q0);
+  }
+  const int i0 = rb * T;
+  if (i0 >= n_b) return false;
+  g.b = b;
+  g.q0 = q0;
+  g.past = past;
+  g.i0 = i0;
+  g.tok_valid = min(T, n_b - i0);
+  const int p_lo = past + i0;
+  const int p_hi = past + i0 + g.tok_valid - 1;
+  const int seq_end = past + n_b;  // positions < seq_end are cached
+  if (err != nullptr && rb == 0 &&
+      static_cast<int64_t>(seq_end) > static_cast<int64_t>(max_blocks) * kBlockSize)
+    flag_error(err, PSW_DEVERR_CAPACITY);
+  g.j_lo = (window > 0) ? max(0, p_lo - window + 1) : 0;
+  g.j_hi = p_hi;
+  g.kt0 = g.j_lo / BN;
+  g.nkt = g.j_hi / BN - g.kt0 + 1;
+  g.last_page = min((seq_end - 1) / kBlockSize, max_blocks - 1);
+  return true;
+}
+
+// ---------------------------------------------------------------- plan
+// One CTA: counts the key tiles of every (sequence, block) unit, orders the
+// units by that count, longest first (a counting sort over kCostBuckets
+// buckets; counts beyond the last bucket share it), and resets the work
+// counter of the main kernel. Length and capacity errors are reported here.
+__global__ void __launch_bounds__(kPlanThreads)
+prefill_plan_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ past_lens,
+                    int n_seqs, int n_q_total, int max_q_len, int max_blocks, int window, int T,
+                    int BN, int max_rb, PlanHeader* hdr, int2* __restrict__ units,
+                    int32_t* err) {
+  __shared__ int cnt[kCostBuckets];
+  __shared__ int warp_tot[kPlanThreads / 32];
+  constexpr int kPer = kCostBuckets / kPlanThreads;  // buckets per thread
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kCostBuckets; i += kPlanThreads) cnt[i] = 0;
+  __syncthreads();
+  const int64_t n_pot = static_cast<int64_t>(n_seqs) * max_rb;
+  for (int64_t u = tid; u < n_pot; u += kPlanThreads) {
+    const int b = static_cast<int>(u / max_rb);
+    const int rb = static_cast<int>(u - static_cast<int64_t>(b) * max_rb);
+    Geom g;
+    if (!unit_geom(b, rb, cu_q, past_lens, n_q_total, max_q_len, max_blocks, window, T, BN, g,
+                   err))
+      continue;
+    atomicAdd(&cnt[min(g.nkt, kCostBuckets - 1)], 1);
+  }
+  __syncthreads();
+  // Descending bucket order: thread t owns buckets kCostBuckets-1-kPer*t and
+  // the kPer - 1 below it; an exclusive scan of the per-thread sums gives the
+  // first list slot of every bucket.
+  int local[kPer];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    local[i] = cnt[kCostBuckets - 1 - (kPer * tid + i)];
+    sum += local[i];
+  }
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix over warps
+  }
+  __syncthreads();
+  int base = warp_tot[wid] + incl - sum;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    cnt[kCostBuckets - 1 - (kPer * tid + i)] = base;  // first slot of this bucket
+    base += local[i];
+  }
+  if (tid == kPlanThreads - 1) hdr->n_units = base;  // the last thread ends at the total
+  __syncthreads();
+  for (int64_t u = tid; u < n_pot; u += kPlanThreads) {
+    const int b = static_cast<int>(u / max_rb);
+    const int rb = static_cast<int>(u - static_cast<int64_t>(b) * max_rb);
+    Geom g;
+    if (!unit_geom(b, rb, cu_q, past_lens, n_q_total, max_q_len, max_blocks, window, T, BN, g,
+                   nullptr))
+      continue;
+    const int pos = atomicAdd(&cnt[min(g.nkt, kCostBuckets - 1)], 1);
+    units[pos] = make_int2(b, rb);
+  }
+  if (tid == 0) hdr->next_item = 0;
+}
+
+// ---------------------------------------------------------------- softcap
+// tanh(y) for |y| <= 1/4: the odd Taylor polynomial through y^7; the first
+// omitted term, 62/2835 y^9, is below 8.3e-8 there.
+__device__ __forceinline__ float tanh_p7(float y) {
+  const float y2 = y * y;
+  const float r = fmaf(fmaf(-17.f / 315.f, y2, 2.f / 15.f), y2, -1.f / 3.f);
+  return fmaf(r * y2, y, y);
+}
+
+// z = A x + c0 + x^3 (C1 + x^2 (C2 + x^2 C3)) on N raw scores x, two per packed
+// register (without softcap C1 = C2 = C3 = 0 and only A x + c0 is formed);
+// every stage runs over 8 pairs before the next so the dependent FMAs of one
+// pair interleave with those of the others.
+template <int N>
+__device__ __forceinline__ void log2_terms(const float* x, uint64_t* z2, bool cap, float A,
+                                           float C1, float C2, float C3, float c0) {
+  constexpr int G = 8;
+  const uint64_t A2 = f2_pack(A, A), c02 = f2_pack(c0, c0);
+  const uint64_t C12 = f2_pack(C1, C1), C22 = f2_pack(C2, C2), C32 = f2_pack(C3, C3);
+#pragma unroll
+  for (int gb = 0; gb < N / 2; gb += G) {
+    uint64_t xx[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) xx[k] = f2_pack(x[2 * (gb + k)], x[2 * (gb + k) + 1]);
+    if (cap) {
+      uint64_t x2[G], x3[G], r[G];
+#pragma unroll
+      for (int k = 0; k < G; ++k) x2[k] = f2_mul(xx[k], xx[k]);
+#pragma unroll
+      for (int k = 0; k < G; ++k) x3[k] = f2_mul(xx[k], x2[k]);
+#pragma unroll
+      for (int k = 0; k < G; ++k) r[k] = f2_fma(C32, x2[k], C22);
+#pragma unroll
+      for (int k = 0; k < G; ++k) r[k] = f2_fma(r[k], x2[k], C12);
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], A2, c02);
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(x3[k], r[k], z2[gb + k]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], A2, c02);
+    }
+  }
+}
+
 __device__ __forceinline__ float tanh_small(float y) {
   const float y2 = y * y;
   float r = -1382.f / 155925.f;
@@ -126,17 +313,6 @@ __device__ __forceinline__ float tanh_small(float y) {
   r = fmaf(r, y2, 2.f / 15.f);
   r = fmaf(r, y2, -1.f / 3.f);
   return fmaf(r * y2, y, y);
-}
-
-// tanh_small on a pair of values (packed fp32 arithmetic).
-__device__ __forceinline__ uint64_t tanh_small2(uint64_t y) {
-  const uint64_t y2 = f2_mul(y, y);
-  uint64_t r = f2_fma(f2_pack(-1382.f / 155925.f, -1382.f / 155925.f), y2,
-                      f2_pack(62.f / 2835.f, 62.f / 2835.f));
-  r = f2_fma(r, y2, f2_pack(-17.f / 315.f, -17.f / 315.f));
-  r = f2_fma(r, y2, f2_pack(2.f / 15.f, 2.f / 15.f));
-  r = f2_fma(r, y2, f2_pack(-1.f / 3.f, -1.f / 3.f));
-  return f2_fma(f2_mul(r, y2), y, y);
 }
 
 // tanh(y) for any y: 1 - 2 / (e^{2|y|} + 1) with the sign restored, the
@@ -148,63 +324,72 @@ __device__ __forceinline__ float tanh_any(float y) {
   return ay <= 0.5f ? tanh_small(y) : big;
 }
 
+// maximum / minimum of N values (N a multiple of 4), two 3-input chains
+template <int N>
+__device__ __forceinline__ float max_of(const float* x) {
+  float a = x[0], b = x[1];
+#pragma unroll
+  for (int i = 2; i + 1 < N; i += 4) {
+    a = max3f(a, x[i], x[i + 1]);
+    b = (i + 3 < N) ? max3f(b, x[i + 2], x[i + 3]) : b;
+  }
+  return fmaxf(a, b);
+}
+template <int N>
+__device__ __forceinline__ float min_of(const float* x) {
+  float a = x[0], b = x[1];
+#pragma unroll
+  for (int i = 2; i + 1 < N; i += 4) {
+    a = min3f(a, x[i], x[i + 1]);
+    b = (i + 3 < N) ? min3f(b, x[i + 2], x[i + 3]) : b;
+  }
+  return fminf(a, b);
+}
+
+// ---------------------------------------------------------------- kernel
 template <int HD, bool KEQV>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                const __grid_constant__ CUtensorMap v_map, const int32_t* __restrict__ cu_q,
                const int32_t* __restrict__ past_lens, const int32_t* __restrict__ block_table,
                int max_blocks, int64_t num_blocks, int n_q_total, int max_q_len, int n_q,
-               int group, int window, float scale, float softcap, float* __restrict__ out,
+               int group, int window, float scale, float softcap, PlanHeader* hdr,
+               const int2* __restrict__ units, float* __restrict__ out,
                float* __restrict__ lse, int32_t* err) {
   using C = Cfg<HD, KEQV>;
   constexpr int BN = C::kBN;
-  constexpr int HALF = C::kHalf;
-  const int T = kRows / group;  // chunk tokens per tile
-  const int rb = blockIdx.x;
-  const int kvh = blockIdx.y / C::kDSplit;
-  const int dh = blockIdx.y - kvh * C::kDSplit;
-  const int b = blockIdx.z;
+  constexpr int KS = C::kKStages;
+  constexpr int VS = C::kVS;
+  const int T = kRows / group;  // chunk tokens per item
+  const int n_kv = n_q / group;
+  const int subs = n_kv * C::kDSplit;  // items per unit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- tile geometry (uniform across the CTA)
-  const int q0 = cu_q[b];
-  int n_b = cu_q[b + 1] - q0;
-  const int past = past_lens[b];
-  if (n_b < 0 || past < 0 || q0 < 0) {
-    if (rb == 0 && threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PSW_DEVERR_LENGTH);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: every thread leaves
+    if (threadIdx.x == 0) flag_error(err, PSW_DEVERR_PIPELINE);
     return;
   }
-  if (n_b > max_q_len || q0 + n_b > n_q_total) {
-    if (rb == 0 && threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PSW_DEVERR_LENGTH);
-    n_b = min(max_q_len, n_q_total - q0);
-  }
-  const int i0 = rb * T;
-  if (i0 >= n_b) return;
-  const int tok_valid = min(T, n_b - i0);
-  const int p_lo = past + i0;
-  const int p_hi = past + i0 + tok_valid - 1;
-  const int seq_end = past + n_b;  // positions < seq_end are cached
-  if (static_cast<int64_t>(seq_end) > static_cast<int64_t>(max_blocks) * kBlockSize) {
-    if (rb == 0 && threadIdx.x == 0 && blockIdx.y == 0) flag_error(err, PSW_DEVERR_CAPACITY);
-  }
-  const int j_lo = (window > 0) ? max(0, p_lo - window + 1) : 0;
-  const int j_hi = p_hi;
-  const int kt0 = j_lo / BN;
-  const int nkt = j_hi / BN - kt0 + 1;
-  const int last_page = min((seq_end - 1) / kBlockSize, max_blocks - 1);
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_raw + pad;
   uint8_t* q_smem = smem;
   uint8_t* k_ring = smem + C::kQBytes;
-  uint8_t* v_ring = k_ring + C::kKStages * C::kKBytes;
+  uint8_t* v_ring = k_ring + KS * C::kKBytes;
   Bars* bars = reinterpret_cast<Bars*>(v_ring + C::kVStages * C::kVBytes);
   static_assert(sizeof(Bars) <= C::kBarsBytes, "barrier block");
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->item_full[i], 1);
+      // readers of an item id: the two MMA threads, the V producer, the
+      // softmax and the epilogue warps
+      mbar_init(&bars->item_empty[i], 2 + (KEQV ? 0 : 1) + kSoftmaxWarps + kEpiWarps);
+      mbar_init(&bars->stats_full[i], kSoftmaxWarps);
+      mbar_init(&bars->stats_free[i], kEpiWarps);
+    }
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < 3; ++i) {
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
     }
@@ -216,12 +401,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       mbar_init(&bars->p_full[i], kSoftmaxWarps);
       mbar_init(&bars->p_free[i], 1);
     }
-    mbar_init(&bars->mma_drained, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_free, kEpiWarps);
+    mbar_init(&bars->mma_drained, 2);  // one commit from each MMA thread
     bars->abort = 0;
-    bars->sm_abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc::alloc(&bars->tmem_base, C::kTmemCols);
     tc::relinquish();
   }
@@ -230,424 +416,563 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   tc::fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
+  const int n_items = hdr->n_units * subs;
 
-  if (warp == kProducerWarp || warp == kVProducerWarp) {
+  // item id -> KV head, head_dim half and geometry of its unit
+  auto item_geom = [&](int item, int& kvh, int& dh, Geom& g) {
+    const int u = item / subs;
+    const int sub = item - u * subs;
+    kvh = sub / C::kDSplit;
+    dh = sub - kvh * C::kDSplit;
+    const int2 unit = units[u];
+    return unit_geom(unit.x, unit.y, cu_q, past_lens, n_q_total, max_q_len, max_blocks, window,
+                     T, BN, g, nullptr);
+  };
+
+  if (warp == kKWarp || warp == kVWarp) {
     // ------------------------------------------------------------ producers
-    const bool v_side = (warp == kVProducerWarp);
+    const bool v_side = (warp == kVWarp);
     if (v_side && KEQV) goto done;  // V is the K tile
     if (!v_side && lane == 0) {
       prefetch_tensormap(&q_map);
       prefetch_tensormap(&k_map);
       if (!KEQV) prefetch_tensormap(&v_map);
-      mbar_arrive_expect_tx(&bars->q_full,
-                            static_cast<uint32_t>(C::kQChunks * group * T * 128));
-      for (int c = 0; c < C::kQChunks; ++c)
-        tma_load_3d(q_smem + c * (kRows * 128), &q_map, &bars->q_full, c * 64, kvh * group,
-                    q0 + i0);
     }
-    // K boxes: lane -> (page, chunk) for lane < pages * kQChunks; V boxes likewise
-    const int k_lp = lane / C::kQChunks, k_lc = lane - k_lp * C::kQChunks;
-    const int v_lp = lane / C::kVChunks, v_lc = lane - v_lp * C::kVChunks;
-    constexpr int kKBoxes = C::kPagesPerTile * C::kQChunks;
-    constexpr int kVBoxes = C::kPagesPerTile * C::kVChunks;
-    // Block ids of this CTA's pages, 32 at a time: lane l holds page
-    // first_page + 32 g + l of group g; the next group is loaded one group
-    // ahead, so a tile needs only shuffles.
     constexpr int P = C::kPagesPerTile;
     constexpr int kTilesPerGroup = 32 / P;
-    const int first_page = kt0 * P;
-    auto load_group = [&](int grp) -> int {
-      const int page = first_page + grp * 32 + lane;
-      if (grp * kTilesPerGroup >= nkt || page > last_page) return -1;
-      int blk = block_table[static_cast<int64_t>(b) * max_blocks + page];
-      if (blk < 0 || blk >= num_blocks) {
-        flag_error(err, PSW_DEVERR_BLOCK_ID);
-        blk = -1;  // out-of-range box: TMA fills zeros
-      }
-      return blk;
-    };
-    int ids = load_group(0), ids_next = load_group(1);
-    const int nst = v_side ? C::kVS : C::kKStages;
-    const int my_lp = v_side ? v_lp : k_lp;
-    int issued = 0;
-    for (int j = 0; j < nkt; ++j, ++issued) {
-      const int stage = j % nst;
-      const uint32_t ph = static_cast<uint32_t>(j / nst) & 1u;
-      if (j > 0 && j % kTilesPerGroup == 0) {
-        ids = ids_next;
-        ids_next = load_group(j / kTilesPerGroup + 1);
-      }
-      const int src = (j % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
-      const int my_blk = __shfl_sync(0xffffffffu, ids, src);
-      const int jp = j + 3;  // tile whose pages are warmed in L2 now
-      const int psrc = (jp % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
-      const int pf_same = __shfl_sync(0xffffffffu, ids, psrc);
-      const int pf_next = __shfl_sync(0xffffffffu, ids_next, psrc);
-      const int pf_blk = (jp / kTilesPerGroup == j / kTilesPerGroup) ? pf_same : pf_next;
-      uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
-      uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(empty, ph ^ 1);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok || *abort_flag) {
-        if (lane == 0) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(full, v_side ? C::kVBytes : C::kKBytes);
-      __syncwarp();
+    constexpr int kKBoxes = P * C::kQChunks;
+    const int k_lp = lane / C::kQChunks, k_lc = lane - k_lp * C::kQChunks;
+    const int nst = v_side ? VS : KS;
+    const int my_lp = v_side ? lane : k_lp;  // V: one whole-page box per lane
+    int gt = 0;  // tiles issued by this warp over all items
+    int nq = 0;  // Q tiles issued
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      // ---- the item: the K warp takes it and publishes it, the V warp reads it
+      int item = -1;
+      const int slot = n & 1;
       if (!v_side) {
-        if (lane < kKBoxes) {
-          tma_load_3d(k_ring + stage * C::kKBytes + k_lc * C::kChunkTileBytes +
-                          k_lp * kPageBoxBytes,
-                      &k_map, full, 0, kvh * C::kQChunks + k_lc, my_blk * kBlockSize);
-          if (jp < nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
-            tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, pf_blk * kBlockSize);
+        if (lane == 0) {
+          if (n >= 2) ok = mbar_wait(&bars->item_empty[slot], ((n >> 1) - 1) & 1);
+          if (ok) {
+            const int it = *abort_flag ? n_items : atomicAdd(&hdr->next_item, 1);
+            item = it < n_items ? it : -1;
+            bars->item[slot] = item;
+            mbar_arrive(&bars->item_full[slot]);
+          }
         }
       } else {
-        if (lane < kVBoxes) {
-          const int y = kvh * C::kQChunks + dh * C::kVChunks + v_lc;
-          tma_load_3d(v_ring + stage * C::kVBytes + v_lc * C::kChunkTileBytes +
-                          v_lp * kPageBoxBytes,
-                      &v_map, full, 0, y, my_blk * kBlockSize);
-          if (jp < nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, y, pf_blk * kBlockSize);
+        ok = mbar_wait(&bars->item_full[slot], (n >> 1) & 1);
+        if (ok) item = bars->item[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (!ok || item < 0) break;
+      int kvh, dh;
+      Geom g;
+      item_geom(item, kvh, dh, g);  // listed units always have rows
+      // ---- Q, once the previous item no longer needs the Q tile
+      if (!v_side) {
+        if (lane == 0) {
+          if (nq > 0)
+            ok = mbar_wait(&bars->q_empty, (nq - 1) & 1);
+          if (ok && !*abort_flag) {
+            mbar_arrive_expect_tx(&bars->q_full,
+                                  static_cast<uint32_t>(C::kQChunks * group * T * 128));
+            for (int c = 0; c < C::kQChunks; ++c)
+              tma_load_3d(q_smem + c * (kRows * 128), &q_map, &bars->q_full, c * 64,
+                          kvh * group, g.q0 + g.i0);
+          } else {
+            ok = false;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++nq;
+      }
+      // ---- K or V tiles. Block ids of the item's pages, 32 at a time: lane l
+      // holds page first_page + 32 grp + l; the next group is read one ahead,
+      // so a tile needs only shuffles.
+      const int first_page = g.kt0 * P;
+      const int32_t* bt_row = block_table + static_cast<int64_t>(g.b) * max_blocks;
+      auto load_group = [&](int grp) -> int {
+        const int page = first_page + grp * 32 + lane;
+        if (grp * kTilesPerGroup >= g.nkt || page > g.last_page) return -1;
+        int blk = bt_row[page];
+        if (blk < 0 || blk >= num_blocks) {
+          flag_error(err, PSW_DEVERR_BLOCK_ID);
+          blk = -1;  // out-of-range box: TMA fills zeros
+        }
+        return blk;
+      };
+      int ids = load_group(0), ids_next = load_group(1);
+      for (int j = 0; j < g.nkt; ++j, ++gt) {
+        const int stage = gt % nst;
+        const uint32_t ph = static_cast<uint32_t>(gt / nst) & 1u;
+        if (j > 0 && j % kTilesPerGroup == 0) {
+          ids = ids_next;
+          ids_next = load_group(j / kTilesPerGroup + 1);
+        }
+        const int src = (j % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
+        const int my_blk = __shfl_sync(0xffffffffu, ids, src);
+        const int jp = j + 3;  // tile whose pages are warmed in L2 now
+        const int psrc = (jp % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
+        const int pf_same = __shfl_sync(0xffffffffu, ids, psrc);
+        const int pf_next = __shfl_sync(0xffffffffu, ids_next, psrc);
+        const int pf_blk = (jp / kTilesPerGroup == j / kTilesPerGroup) ? pf_same : pf_next;
+        uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
+        uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
+        if (lane == 0) ok = mbar_wait(empty, ph ^ 1) && !*abort_flag;
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(full, v_side ? C::kVBytes : C::kKBytes);
+        __syncwarp();
+        if (!v_side) {
+          if (lane < kKBoxes) {
+            tma_load_3d(k_ring + stage * C::kKBytes + k_lc * C::kChunkTileBytes +
+                            k_lp * kPageBoxBytes,
+                        &k_map, full, 0, kvh * C::kQChunks + k_lc, my_blk * kBlockSize);
+            if (jp < g.nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
+              tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, pf_blk * kBlockSize);
+          }
+        } else {
+          if (lane < P) {  // V tile: [page][chunk][16 rows][128 B]
+            const int z = kvh * C::kQChunks + dh * C::kVChunks;
+            tma_load_3d(v_ring + stage * C::kVBytes + lane * C::kVPageBytes, &v_map, full, 0,
+                        my_blk * kBlockSize, z);
+            if (jp < g.nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, pf_blk * kBlockSize, z);
+          }
         }
       }
     }
+    if (!ok && lane == 0) {
+      flag_error(err, PSW_DEVERR_PIPELINE);
+      *abort_flag = 1;
+    }
     if (lane == 0) {  // drain this warp's own copies before anyone leaves
-      if (!v_side) mbar_wait(&bars->q_full, 0);
-      for (int i = max(0, issued - nst); i < issued; ++i)
+      if (!v_side && nq > 0) mbar_wait(&bars->q_full, (nq - 1) & 1);
+      for (int i = max(0, gt - nst); i < gt; ++i)
         mbar_wait(v_side ? &bars->v_full[i % nst] : &bars->k_full[i % nst],
                   static_cast<uint32_t>(i / nst) & 1u);
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kQkWarp || warp == kPvWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two warps issue tcgen05.mma, one elected thread each: warp kQkWarp the
+    // QK stream S_g = Q K_g^T (into S buffer g mod 2, once the softmax has read
+    // the S of tile g - 2 and K_g has landed), warp kPvWarp the PV stream
+    // O += P_g V_g (once P_g is in tensor memory and V_g has landed). Each
+    // stream depends only on earlier tiles, a commit tracks only its own
+    // thread's MMAs, and the tensor pipe interleaves the two streams.
+    // Descriptors are a base plus compile-time offsets (the 14-bit address
+    // field never carries: shared addresses stay below 2^18).
+    const bool qk_side = (warp == kQkWarp);
     if (lane == 0) {
       const uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, BN, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, C::kOCols, 0, 1);
-      const uint32_t q_base = smem_u32(q_smem);
+      const uint64_t q_desc = tc::smem_desc(smem_u32(q_smem), 16, 1024, tc::kSwizzle128B);
       const uint32_t k_base = smem_u32(k_ring);
       const uint32_t v_base = smem_u32(v_ring);
-      bool ok = mbar_wait(&bars->q_full, 0);
-      // Non-blocking scheduler: issue QK_j as soon as K_j has landed and its S
-      // buffer is free (at most two ahead of the softmax), PV_i as soon as P_i
-      // is in TMEM and V_i has landed; QK first, so S is ready before the
-      // softmax asks for it. The tensor pipe runs the MMAs in issue order.
-      int next_qk = 0, next_pv = 0;
-      long long idle_since = clock64();
-      while (ok && next_pv < nkt) {
-        bool progressed = false;
-        if (next_qk < nkt && next_qk < next_pv + 2) {
-          const int j = next_qk, sb = j & 1;
-          if (mbar_try_wait(&bars->k_full[stage_of<C::kKStages>(j)], round_of<C::kKStages>(j)) &&
-              (j < 2 || mbar_try_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1))) {
-            tc::fence_after();
-            const uint32_t kb = k_base + stage_of<C::kKStages>(j) * C::kKBytes;
-            #pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              const int c = ks >> 2;
-              const uint64_t adesc = tc::smem_desc(q_base + c * (kRows * 128) + (ks & 3) * 32,
-                                                   16, 1024, tc::kSwizzle128B);
-              const uint64_t bdesc = tc::smem_desc(kb + c * C::kChunkTileBytes + (ks & 3) * 32,
-                                                   16, 1024, tc::kSwizzle128B);
-              tc::mma_ss(tmem + C::kTmemS + sb * BN, adesc, bdesc, idesc_qk, ks > 0 ? 1u : 0u);
-            }
-            tc::commit(&bars->s_full[sb]);
-            if (!KEQV) tc::commit(&bars->k_empty[stage_of<C::kKStages>(j)]);  // K read by QK
-            ++next_qk;
-            progressed = true;
+      bool ok = true;
+      int g_tile = 0;
+      for (int n = 0; ok; ++n) {
+        ok = mbar_wait(&bars->item_full[n & 1], (n >> 1) & 1);
+        if (!ok) break;
+        const int item = bars->item[n & 1];
+        mbar_arrive(&bars->item_empty[n & 1]);
+        if (item < 0) break;
+        int kvh, dh;
+        Geom g;
+        item_geom(item, kvh, dh, g);
+        for (int j = 0; j < g.nkt && ok; ++j, ++g_tile) {
+          const bool first = (j == 0), last = (j == g.nkt - 1);
+          if (*abort_flag) {
+            ok = false;
+            break;
           }
-        }
-        if (!progressed && next_pv < next_qk) {
-          const int i = next_pv, pb = i & 1;
-          if (mbar_try_wait(&bars->p_full[pb], (i >> 1) & 1) &&
-              (KEQV || mbar_try_wait(&bars->v_full[stage_of<C::kVS>(i)], round_of<C::kVS>(i)))) {
+          if (qk_side) {
+            const int stage = g_tile % KS;
+            ok = (!first || mbar_wait(&bars->q_full, n & 1)) &&
+                 mbar_wait(&bars->k_full[stage], (g_tile / KS) & 1) &&
+                 (g_tile < 2 ||
+                  mbar_wait(&bars->s_free[g_tile & 1], ((g_tile >> 1) - 1) & 1));
+            if (!ok) break;
             tc::fence_after();
-            const uint32_t vb =
-                KEQV ? k_base + stage_of<C::kKStages>(i) * C::kKBytes +
-                           dh * C::kVChunks * C::kChunkTileBytes
-                     : v_base + stage_of<C::kVS>(i) * C::kVBytes;
+            const uint64_t k_desc =
+                tc::smem_desc(k_base + stage * C::kKBytes, 16, 1024, tc::kSwizzle128B);
+            const uint32_t d = tmem + C::kTmemS + (g_tile & 1) * BN;
+#pragma unroll
+            for (int ks = 0; ks < HD / 16; ++ks) {
+              constexpr int kQChunkBytes = kRows * 128;
+              const uint32_t off_q =
+                  static_cast<uint32_t>((ks >> 2) * kQChunkBytes + (ks & 3) * 32) >> 4;
+              const uint32_t off_k =
+                  static_cast<uint32_t>((ks >> 2) * C::kChunkTileBytes + (ks & 3) * 32) >> 4;
+              tc::mma_ss(d, q_desc + off_q, k_desc + off_k, idesc_qk, ks > 0 ? 1u : 0u);
+            }
+            tc::commit(&bars->s_full[g_tile & 1]);
+            if (!KEQV) tc::commit(&bars->k_empty[stage]);  // K read by QK
+            if (last) tc::commit(&bars->q_empty);          // the Q tile may be replaced
+          } else {
+            const int pb = g_tile & 1;
+            ok = mbar_wait(&bars->p_full[pb], (g_tile >> 1) & 1) &&
+                 (KEQV || mbar_wait(&bars->v_full[g_tile % VS], (g_tile / VS) & 1)) &&
+                 (!first || n == 0 || mbar_wait(&bars->o_free, (n - 1) & 1));
+            if (!ok) break;
+            tc::fence_after();
+            // V with k_eq_v is the K tile ([chunk][page][16 rows]); a V tile of
+            // its own is [page][chunk][16 rows]; a K16 step is one page either way
+            const uint32_t vb = KEQV ? k_base + (g_tile % KS) * C::kKBytes +
+                                           dh * C::kVChunks * C::kChunkTileBytes
+                                     : v_base + (g_tile % VS) * C::kVBytes;
+            const uint64_t v_desc = tc::smem_desc(vb, KEQV ? C::kChunkTileBytes : kPageBoxBytes,
+                                                  1024, tc::kSwizzle128B);
+            constexpr int kPageStep = KEQV ? kPageBoxBytes : C::kVPageBytes;
             const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
-            #pragma unroll
+#pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
-              const uint64_t bdesc = tc::smem_desc(vb + ks * 16 * 128, C::kChunkTileBytes, 1024,
-                                                   tc::kSwizzle128B);
+              const uint64_t bdesc = v_desc + static_cast<uint32_t>((ks * kPageStep) >> 4);
               tc::mma_ts(tmem + C::kTmemO, p_hi + ks * 8, bdesc, idesc_pv,
-                         (i > 0 || ks > 0) ? 1u : 0u);
+                         (!first || ks > 0) ? 1u : 0u);
               tc::mma_ts(tmem + C::kTmemO, p_hi + BN / 2 + ks * 8, bdesc, idesc_pv, 1u);
             }
             tc::commit(&bars->p_free[pb]);
-            // V (or, with k_eq_v, the whole K part) of this stage is free once PV ends
-            tc::commit(KEQV ? &bars->k_empty[stage_of<C::kKStages>(i)]
-                            : &bars->v_empty[stage_of<C::kVS>(i)]);
-            ++next_pv;
-            progressed = true;
+            // V (or, with k_eq_v, the whole K stage) is free once PV ends
+            tc::commit(KEQV ? &bars->k_empty[g_tile % KS] : &bars->v_empty[g_tile % VS]);
+            if (last) tc::commit(&bars->o_full);  // the item's O is final
           }
         }
-        if (progressed) {
-          idle_since = clock64();
-        } else if (*abort_flag || clock64() - idle_since > kWaitLimitCycles) {
-          ok = false;
-        }
       }
-      if (!ok) { flag_error(err, PSW_DEVERR_PIPELINE); *abort_flag = 1; }
+      if (!ok) {
+        flag_error(err, PSW_DEVERR_PIPELINE);
+        *abort_flag = 1;
+      }
       // every MMA this thread issued has finished before tensor memory is freed
       tc::commit(&bars->mma_drained);
       mbar_wait(&bars->mma_drained, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3;       // TMEM lane quadrant = rows 32*quad ...
-    const int half = warp >> 2;      // key columns [half*HALF, (half+1)*HALF)
+    // Warp w owns the 32 rows of tensor-memory lane quadrant w and every key
+    // column of a tile: a row's maximum and sum stay inside one thread.
+    const int quad = warp;
     const int r = quad * 32 + lane;  // tile row
     const int t = r / group;
-    const int h = r - t * group;
-    const bool row_ok = (t < tok_valid) && (r < group * T);
-    const int p = past + i0 + t;
-    const int vis_lo = (window > 0) ? max(0, p - window + 1) : 0;  // this row sees [vis_lo, p]
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const bool use_cap = softcap > 0.f;
-    const float inv_cap = use_cap ? 1.f / softcap : 0.f;
-    const float scale_l2 = scale * kLog2e;
-    const float mul = use_cap ? softcap * kLog2e : 1.f;  // log2-domain value of the proxy
-    float m_run = -INFINITY, l_run = 0.f;
-    volatile int* sm_abort = &bars->sm_abort;
-    const uint32_t pair_bar = 1 + quad;  // named barrier of warps quad and quad + 4
-    for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      // every decision below is warp-uniform; the abort decision is taken by all
-      // softmax warps together after the named barrier at the end of the tile
-      bool okw = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1));
-      const int key0 = (kt0 + j) * BN + half * HALF;
-      float x[HALF];
-      float alpha = 1.f;
-      if (okw) {
+    const float sc = use_cap ? scale / softcap : 0.f;               // y = s_raw * sc
+    const float mul = use_cap ? softcap * kLog2e : scale * kLog2e;  // log2-domain factor
+    const uint64_t mul2 = f2_pack(mul, mul);
+    // x-domain coefficients: A x + x^3 (C1 + x^2 (C2 + x^2 C3)) = mul tanh(x sc)
+    // to the y^7 term (with softcap), A x = mul x without
+    const float A = use_cap ? sc * mul : mul;
+    const float B = sc * sc;
+    const float C1 = A * B * (-1.f / 3.f);
+    const float C2 = A * B * B * (2.f / 15.f);
+    const float C3 = A * B * B * B * (-17.f / 315.f);
+    int g_tile = 0;  // global tile counter (S/P buffers, K/V stages)
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int slot = n & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[slot], (n >> 1) & 1));
+      const int item = ok ? bars->item[slot] : -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+      if (!ok || item < 0) break;
+      int kvh, dh;
+      Geom g;
+      item_geom(item, kvh, dh, g);
+      const bool row_ok = t < g.tok_valid;
+      const int p = g.past + g.i0 + t;
+      const int vis_lo = (window > 0) ? max(0, p - window + 1) : 0;  // row sees [vis_lo, p]
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < g.nkt; ++j, ++g_tile) {
+        const int sb = g_tile & 1;
+        // every decision below is warp-uniform
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g_tile >> 1) & 1)) &&
+             !*abort_flag;
+        if (!ok) break;
         tc::fence_after();
+        float x[BN];
         {
-          uint32_t v[HALF];
-          #pragma unroll
-          for (int c16 = 0; c16 < HALF / 16; ++c16)
-            tc::ld16(tmem + lane_off + C::kTmemS + sb * BN + half * HALF + c16 * 16,
+          uint32_t v[BN];
+#pragma unroll
+          for (int c16 = 0; c16 < BN / 16; ++c16)
+            tc::ld16(tmem + lane_off + C::kTmemS + sb * BN + c16 * 16,
                      *reinterpret_cast<uint32_t(*)[16]>(&v[c16 * 16]));
           tc::wait_ld();
-          #pragma unroll
-          for (int i = 0; i < HALF; ++i) x[i] = __uint_as_float(v[i]);
+#pragma unroll
+          for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(v[i]);
         }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-        // scores to a monotone proxy u with log2-domain value mul * u: the tanh
-        // of the softcap (mul = cap log2 e) or the scaled score (mul = 1);
-        // every loop is branch-free
-        if (use_cap) {
-          const float sc = scale * inv_cap;
-          const uint64_t sc2 = f2_pack(sc, sc);
-          float amax = 0.f;
-          #pragma unroll
-          for (int i = 0; i < HALF / 2; ++i) {
-            const float2 y = f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), sc2));
-            x[2 * i] = y.x;
-            x[2 * i + 1] = y.y;
-            amax = fmaxf(amax, fmaxf(fabsf(y.x), fabsf(y.y)));
+        const int key0 = (g.kt0 + j) * BN;
+        const bool interior =
+            __all_sync(0xffffffffu, row_ok && key0 >= vis_lo && key0 + BN - 1 <= p);
+        // z: log2-domain exponent of P (score minus the running maximum).
+        // Fast path (interior tile, every |s/cap| of the warp's tile <= 1/4):
+        // the row maximum comes from the raw maximum (the softcap is monotone)
+        // and z = x A - m + x^3 r(x^2), the odd Taylor polynomial of tanh
+        // through y^7 (next term below 8.3e-8) with the scale, the softcap and
+        // log2 e folded into its coefficients: six packed FMAs per pair.
+        // Otherwise (edge tiles, larger |s/cap|) the capped scores are formed
+        // first, hidden keys are set to -inf, and their maximum is taken.
+        uint64_t z2[BN / 2];
+        float alpha = 1.f;
+        {
+          const float mx = max_of<BN>(x);
+          bool poly_ok = true;
+          if (use_cap) {
+            const float mn = min_of<BN>(x);
+            poly_ok = __all_sync(0xffffffffu, fmaxf(mx, -mn) * sc <= 0.25f);
           }
-          if (__any_sync(0xffffffffu, amax > 0.5f)) {
-            #pragma unroll
-            for (int k = 0; k < HALF; ++k) x[k] = tanh_any(x[k]);
+          const bool fast = interior && poly_ok;
+          float tmax = 0.f;
+          if (fast) tmax = use_cap ? mul * tanh_p7(mx * sc) : mx * mul;
+          if (fast) {
+            if (tmax > m_run + kRescaleThreshold) {  // lazy rescale (also the first key)
+              alpha = ex2_approx(m_run - tmax);
+              m_run = tmax;
+            }
+            log2_terms<BN>(x, z2, use_cap, A, C1, C2, C3, -m_run);
           } else {
-            #pragma unroll
-            for (int i = 0; i < HALF / 2; ++i) {
-              const float2 t = f2_unpack(tanh_small2(f2_pack(x[2 * i], x[2 * i + 1])));
-              x[2 * i] = t.x;
-              x[2 * i + 1] = t.y;
+            if (use_cap && poly_ok) {
+              log2_terms<BN>(x, z2, true, A, C1, C2, C3, 0.f);
+            } else if (use_cap) {
+#pragma unroll
+              for (int i = 0; i < BN / 2; ++i)
+                z2[i] = f2_pack(mul * tanh_any(x[2 * i] * sc), mul * tanh_any(x[2 * i + 1] * sc));
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 2; ++i) z2[i] = f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), mul2);
             }
-          }
-        } else {
-          const uint64_t s2 = f2_pack(scale_l2, scale_l2);
-          #pragma unroll
-          for (int i = 0; i < HALF / 2; ++i) {
-            const float2 t = f2_unpack(f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), s2));
-            x[2 * i] = t.x;
-            x[2 * i + 1] = t.y;
+            float uu[BN];
+#pragma unroll
+            for (int i = 0; i < BN / 2; ++i) {
+              const float2 w = f2_unpack(z2[i]);
+              const int k0 = key0 + 2 * i;
+              uu[2 * i] = (row_ok && k0 >= vis_lo && k0 <= p) ? w.x : -INFINITY;
+              uu[2 * i + 1] = (row_ok && k0 + 1 >= vis_lo && k0 + 1 <= p) ? w.y : -INFINITY;
+            }
+            tmax = max_of<BN>(uu);
+            if (tmax > m_run + kRescaleThreshold) {
+              alpha = ex2_approx(m_run - tmax);
+              m_run = tmax;
+            }
+            const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+            const uint64_t negm2 = f2_pack(-m_use, -m_use);
+#pragma unroll
+            for (int i = 0; i < BN / 2; ++i)
+              z2[i] = f2_add(f2_pack(uu[2 * i], uu[2 * i + 1]), negm2);
           }
         }
-        // band + causal predicate only where the tile straddles this row's edges
-        const bool interior = row_ok && key0 >= vis_lo && key0 + HALF - 1 <= p;
-        if (!__all_sync(0xffffffffu, interior)) {
-          #pragma unroll
-          for (int k = 0; k < HALF; ++k) {
-            const int key = key0 + k;
-            x[k] = (row_ok && key >= vis_lo && key <= p) ? x[k] : -INFINITY;
-          }
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        #pragma unroll
-        for (int k = 0; k < HALF; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
-        bars->red[half][r] = mul * fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      }
-      named_bar_sync(pair_bar, 64);  // the two halves of these rows meet
-      if (okw) {
-        const float m_tile = fmaxf(bars->red[0][r], bars->red[1][r]);
-        if (m_tile > m_run + kRescaleThreshold) {  // lazy rescale (also the first visible key)
-          alpha = ex2_approx(m_run - m_tile);
-          m_run = m_tile;
-        }
-        // rescaling O needs PV_{j-1} finished; each warp of the pair takes half of O
+        // rescaling O needs the item's previous PV finished
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          okw = __all_sync(0xffffffffu,
-                           mbar_wait(&bars->p_free[(j - 1) & 1], ((j - 1) >> 1) & 1));
+          const int gprev = g_tile - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free[gprev & 1], (gprev >> 1) & 1));
+          if (!ok) break;
           tc::fence_after();
-          if (okw) {
-            #pragma unroll 1
-            for (int c16 = 0; c16 < C::kOCols / 32; ++c16) {
-              const uint32_t col = tmem + lane_off + C::kTmemO + half * (C::kOCols / 2) + c16 * 16;
-              uint32_t v[16];
-              tc::ld16(col, v);
-              tc::wait_ld();
-              #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tc::st16(col, v);
-            }
-            tc::wait_st();
+#pragma unroll 1
+          for (int c16 = 0; c16 < C::kOCols / 16; ++c16) {
+            const uint32_t col = tmem + lane_off + C::kTmemO + c16 * 16;
+            uint32_t v[16];
+            tc::ld16(col, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tc::st16(col, v);
           }
+          tc::wait_st();
         }
-      }
-      if (okw) {
-        // zero V rows that no row of this tile can see (first / last key tile)
-        if (j == 0 || j == nkt - 1) {
-          const int tkey0 = (kt0 + j) * BN;
-          uint8_t* vt = KEQV ? k_ring + stage_of<C::kKStages>(j) * C::kKBytes +
-                                   dh * C::kVChunks * C::kChunkTileBytes
-                             : v_ring + stage_of<C::kVS>(j) * C::kVBytes;
-          const int z_lo = max(0, j_lo - tkey0);       // rows [0, z_lo) hidden
-          const int z_hi = min(BN, j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
-          if (!KEQV && (z_lo > 0 || z_hi < BN))  // V may land after K
-            okw = __all_sync(0xffffffffu, mbar_wait(&bars->v_full[stage_of<C::kVS>(j)],
-                                                    round_of<C::kVS>(j)));
-          if (okw && (z_lo > 0 || z_hi < BN)) {
+        // zero V rows that no row of this item can see (its first / last key tile)
+        if (j == 0 || j == g.nkt - 1) {
+          const int tkey0 = (g.kt0 + j) * BN;
+          const int z_lo = max(0, g.j_lo - tkey0);       // rows [0, z_lo) hidden
+          const int z_hi = min(BN, g.j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
+          if (z_lo > 0 || z_hi < BN) {
+            uint8_t* vt = KEQV ? k_ring + (g_tile % KS) * C::kKBytes +
+                                     dh * C::kVChunks * C::kChunkTileBytes
+                               : v_ring + (g_tile % VS) * C::kVBytes;
+            if (!KEQV) {  // V may land after K
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->v_full[g_tile % VS], (g_tile / VS) & 1));
+              if (!ok) break;
+            }
             for (int idx = threadIdx.x; idx < C::kVChunks * BN * 8; idx += kSoftmaxWarps * 32) {
               const int cv = idx / (BN * 8);
               const int rem = idx - cv * (BN * 8);
-              const int row = rem >> 3, u = rem & 7;
+              const int row = rem >> 3, uu = rem & 7;
+              const int off = KEQV ? cv * C::kChunkTileBytes + row * 128
+                                   : (row >> 4) * C::kVPageBytes + cv * kPageBoxBytes +
+                                         (row & 15) * 128;
               if (row < z_lo || row >= z_hi)
-                *reinterpret_cast<uint4*>(vt + cv * C::kChunkTileBytes + row * 128 + u * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(vt + off + uu * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
           }
         }
-        // P_{j-2} must have been multiplied in before its buffer is rewritten
-        if (j >= 2)
-          okw = __all_sync(0xffffffffu,
-                           mbar_wait(&bars->p_free[sb], ((j >> 1) - 1) & 1));
-      }
-      if (okw) {
-        // P = 2^(x - m): bf16 high part and bf16 remainder into tensor memory
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        const uint64_t mul2 = f2_pack(mul, mul), negm2 = f2_pack(-m_use, -m_use);
-        uint64_t ps2[2] = {0ull, 0ull};
-        uint32_t hi[HALF / 2], lo[HALF / 2];
-        #pragma unroll
-        for (int i = 0; i < HALF / 2; ++i) {
-          const float2 z = f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), mul2, negm2));
-          const float a = ex2_approx(z.x), bb = ex2_approx(z.y);
-          const uint64_t ab = f2_pack(a, bb);
-          ps2[i & 1] = f2_add(ps2[i & 1], ab);
-          // P = hi + lo without conversion instructions: hi keeps the upper 16
-          // bits of P (bf16 by truncation), lo = P - hi exactly, then truncated
-          // to bf16 the same way; together they carry P to 2^-14 relative.
-          const uint32_t ha = __float_as_uint(a) & 0xFFFF0000u;
-          const uint32_t hb = __float_as_uint(bb) & 0xFFFF0000u;
-          hi[i] = __byte_perm(ha, hb, 0x7632);
-          const float2 l = f2_unpack(f2_sub(ab, f2_pack(__uint_as_float(ha), __uint_as_float(hb))));
-          lo[i] = __byte_perm(__float_as_uint(l.x), __float_as_uint(l.y), 0x7632);
+        // P_{g-2} must have been multiplied in before its buffer is rewritten
+        if (g_tile >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free[sb], ((g_tile >> 1) - 1) & 1));
+          if (!ok) break;
         }
-        const float2 ps_a = f2_unpack(ps2[0]), ps_b = f2_unpack(ps2[1]);
-        float ps[4] = {ps_a.x, ps_a.y, ps_b.x, ps_b.y};
-        const uint32_t pcol = tmem + lane_off + C::kTmemP + sb * BN + half * (HALF / 2);
-        if constexpr (HALF / 2 == 16) {
-          tc::st16(pcol, hi);
-          tc::st16(pcol + BN / 2, lo);
-        } else {
-          tc::st8(pcol, hi);
-          tc::st8(pcol + BN / 2, lo);
+        {
+          // P = 2^z: bf16 high part and bf16 remainder into tensor memory, 16
+          // column pairs at a time, each stage over 8 pairs before the next
+          uint64_t ps2[2] = {0ull, 0ull};
+          constexpr int kChunkPairs = (BN / 2 < 16) ? BN / 2 : 16;
+          constexpr int G = 8;
+#pragma unroll
+          for (int c = 0; c < BN / 2 / kChunkPairs; ++c) {
+            uint32_t hi[kChunkPairs], lo[kChunkPairs];
+#pragma unroll
+            for (int gb = 0; gb < kChunkPairs; gb += G) {
+              float pa[G], pb[G];
+#pragma unroll
+              for (int k = 0; k < G; ++k) {
+                const float2 z = f2_unpack(z2[c * kChunkPairs + gb + k]);
+                pa[k] = ex2_approx(z.x);
+                pb[k] = ex2_approx(z.y);
+              }
+#pragma unroll
+              for (int k = 0; k < G; ++k) {
+                const uint64_t ab = f2_pack(pa[k], pb[k]);
+                ps2[k & 1] = f2_add(ps2[k & 1], ab);
+                // P = hi + lo without conversion instructions: hi keeps the
+                // upper 16 bits of P (bf16 by truncation), lo = P - hi exactly,
+                // then truncated to bf16 the same way; together they carry P to
+                // 2^-14 relative.
+                hi[gb + k] = __byte_perm(__float_as_uint(pa[k]), __float_as_uint(pb[k]), 0x7632);
+                const uint32_t ha = __float_as_uint(pa[k]) & 0xFFFF0000u;
+                const uint32_t hb = __float_as_uint(pb[k]) & 0xFFFF0000u;
+                const float2 l =
+                    f2_unpack(f2_sub(ab, f2_pack(__uint_as_float(ha), __uint_as_float(hb))));
+                lo[gb + k] = __byte_perm(__float_as_uint(l.x), __float_as_uint(l.y), 0x7632);
+              }
+            }
+            const uint32_t pcol = tmem + lane_off + C::kTmemP + sb * BN + c * kChunkPairs;
+            if constexpr (kChunkPairs == 16) {
+              tc::st16(pcol, hi);
+              tc::st16(pcol + BN / 2, lo);
+            } else {
+              tc::st8(pcol, *reinterpret_cast<uint32_t(*)[8]>(hi));
+              tc::st8(pcol + BN / 2, *reinterpret_cast<uint32_t(*)[8]>(lo));
+            }
+          }
+          const float2 ps_a = f2_unpack(ps2[0]), ps_b = f2_unpack(ps2[1]);
+          l_run = l_run * alpha + ((ps_a.x + ps_a.y) + (ps_b.x + ps_b.y));
+          tc::wait_st();
+          tc::fence_before();
         }
-        l_run = l_run * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-        tc::wait_st();
-        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[sb]);
       }
-      if (!okw && lane == 0) {
-        flag_error(err, PSW_DEVERR_PIPELINE);
-        *sm_abort = 1;
+      if (!ok) break;
+      // row maximum and sum for the epilogue warps (double-buffered by item)
+      if (n >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->stats_free[slot], ((n >> 1) - 1) & 1));
+        if (!ok) break;
       }
-      named_bar_sync(9, kSoftmaxWarps * 32);  // all softmax warps: V zeroing done, abort agreed
-      if (*sm_abort) break;
-      if (lane == 0) mbar_arrive(&bars->p_full[sb]);
+      bars->stat_m[slot][r] = m_run;
+      bars->stat_l[slot][r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->stats_full[slot]);
     }
-    bool ok = !*sm_abort;
-
-    // epilogue: l from both halves, O / l staged through shared memory (the Q
-    // tile and the K/V rings are idle once the last PV is done) and written out
-    // as whole rows with coalesced stores, lse
-    bars->red[half][r] = l_run;
-    if (ok) ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->p_free[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1));
-    named_bar_sync(pair_bar, 64);
-    tc::fence_after();
-    const float l_tot = bars->red[0][r] + bars->red[1][r];
-    const float inv_l = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
-    // staging rows of kOCols floats plus 16 bytes of padding: 32 lanes storing
-    // 16 bytes each at the same column of 32 rows then take the minimum four
-    // shared-memory wavefronts
-    constexpr int kORow = C::kOCols * 4 + 16;
-    static_assert(kRows * kORow <= C::kQBytes + C::kKStages * C::kKBytes +
-                                       C::kVStages * C::kVBytes,
-                  "O staging fits in the Q tile and the K/V rings");
-    uint8_t* ostage = q_smem;  // Q, then the K and V rings: contiguous and idle now
-    if (ok) {
-      #pragma unroll 1
-      for (int c16 = 0; c16 < C::kOCols / 32; ++c16) {
-        const int col0 = half * (C::kOCols / 2) + c16 * 16;
-        uint32_t v[16];
-        tc::ld16(tmem + lane_off + C::kTmemO + col0, v);
-        tc::wait_ld();
-        #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float4 w;
-          w.x = __uint_as_float(v[4 * q4 + 0]) * inv_l;
-          w.y = __uint_as_float(v[4 * q4 + 1]) * inv_l;
-          w.z = __uint_as_float(v[4 * q4 + 2]) * inv_l;
-          w.w = __uint_as_float(v[4 * q4 + 3]) * inv_l;
-          *reinterpret_cast<float4*>(ostage + r * kORow + (col0 + 4 * q4) * 4) = w;
-        }
-      }
-      if (row_ok && dh == 0 && half == 0 && lse != nullptr)
-        lse[static_cast<int64_t>(q0 + i0 + t) * n_q + kvh * group + h] =
-            (l_tot > 0.f) ? (m_run + log2f(l_tot)) * kLn2 : -INFINITY;
-    } else if (lane == 0) {
+    if (!ok && lane == 0) {
       flag_error(err, PSW_DEVERR_PIPELINE);
-      *abort_flag = 1;  // stops the producer and the MMA issuer
+      *abort_flag = 1;
     }
-    named_bar_sync(9, kSoftmaxWarps * 32);  // the whole O tile is staged
-    if (ok) {
-      // warp w copies rows w, w + 8, ...: 32 lanes x 16 bytes per store
-      const int rows_valid = min(group * T, tok_valid * group);
-      for (int rr = warp; rr < rows_valid; rr += kSoftmaxWarps) {
-        const int tt = rr / group, hh = rr - tt * group;
-        float* orow = out + (static_cast<int64_t>(q0 + i0 + tt) * n_q + kvh * group + hh) * HD +
-                      dh * C::kOCols;
-        #pragma unroll
-        for (int c = lane; c < C::kOCols / 4; c += 32)
-          reinterpret_cast<float4*>(orow)[c] =
-              *reinterpret_cast<const float4*>(ostage + rr * kORow + c * 16);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // Warp 4 + q writes the O rows of lane quadrant q once the item's last PV
+    // is done, straight from tensor memory: each 16-lane half is read 32
+    // columns at a time in the 16x256b shape, where four consecutive lanes
+    // hold 8 consecutive columns of one row, so every store writes whole
+    // 32-byte sectors; O is scaled by 1/l, lse = m + ln l. Meanwhile the
+    // softmax warps already work on the next item.
+    const int quad = warp - kSoftmaxWarps;  // = warp mod 4: its lane quadrant
+    const int r = quad * 32 + lane;
+    const int t = r / group;
+    const int h = r - t * group;
+    bool ok = true;
+    for (int n = 0; ok; ++n) {
+      const int slot = n & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[slot], (n >> 1) & 1));
+      const int item = ok ? bars->item[slot] : -1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->item_empty[slot]);
+      if (!ok || item < 0) break;
+      int kvh, dh;
+      Geom g;
+      item_geom(item, kvh, dh, g);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_full, n & 1)) &&
+           __all_sync(0xffffffffu, mbar_wait(&bars->stats_full[slot], (n >> 1) & 1)) &&
+           !*abort_flag;
+      if (!ok) break;
+      // this lane's own row (lse) and the four rows it stores (two per half)
+      const float m_row = bars->stat_m[slot][r];
+      const float l_row = bars->stat_l[slot][r];
+      float inv[4];
+      float* orow[4];
+      bool valid[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tr = quad * 32 + (e >> 1) * 16 + (e & 1) * 8 + (lane >> 2);
+        const float lr = bars->stat_l[slot][tr];
+        inv[e] = (lr > 0.f) ? 1.f / lr : 0.f;
+        const int tt = tr / group, hh = tr - tt * group;
+        valid[e] = tt < g.tok_valid;
+        orow[e] = out + (static_cast<int64_t>(g.q0 + g.i0 + tt) * n_q + kvh * group + hh) * HD +
+                  dh * C::kOCols + 2 * (lane & 3);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->stats_free[slot]);
+      if (t < g.tok_valid && dh == 0 && lse != nullptr)
+        lse[static_cast<int64_t>(g.q0 + g.i0 + t) * n_q + kvh * group + h] =
+            (l_row > 0.f) ? (m_row + log2f(l_row)) * kLn2 : -INFINITY;
+      tc::fence_after();
+#pragma unroll 1
+      for (int cb = 0; cb < C::kOCols / 32; ++cb) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[16];
+          tc::ld16x256_x4(tmem + (static_cast<uint32_t>(quad * 32 + hf * 16) << 16) +
+                              C::kTmemO + cb * 32,
+                          v);
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int e = hf * 2 + e2;
+              if (valid[e]) {
+                float2 w;
+                w.x = __uint_as_float(v[4 * k + 2 * e2]) * inv[e];
+                w.y = __uint_as_float(v[4 * k + 2 * e2 + 1]) * inv[e];
+                *reinterpret_cast<float2*>(orow[e] + cb * 32 + 8 * k) = w;
+              }
+            }
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free);
+    }
+    if (!ok && lane == 0) {
+      flag_error(err, PSW_DEVERR_PIPELINE);
+      *abort_flag = 1;
     }
   }
 
 done:
   tc::fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc::fence_after();
     tc::dealloc(tmem, C::kTmemCols);
   }
@@ -657,7 +982,8 @@ template <int HD, bool KEQV>
 int launch(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_map,
            const CUtensorMap& v_map, const int32_t* cu_q, const int32_t* past_lens, int n_seqs,
            int n_q_total, int max_q_len, const int32_t* block_table, int max_blocks,
-           int64_t num_blocks, float* out, float* lse, int32_t* err, cudaStream_t stream) {
+           int64_t num_blocks, float* out, float* lse, void* ws, int num_sms, int32_t* err,
+           cudaStream_t stream) {
   using C = Cfg<HD, KEQV>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -669,33 +995,49 @@ int launch(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_ma
     attr_set[dev] = true;
   }
   const int T = kRows / L.group();
-  dim3 grid((max_q_len + T - 1) / T, L.n_kv * C::kDSplit, n_seqs);
+  const int max_rb = (max_q_len + T - 1) / T;
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
+  int2* units = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(ws) + sizeof(PlanHeader));
+  prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu_q, past_lens, n_seqs, n_q_total,
+                                                      max_q_len, max_blocks, L.window, T, C::kBN,
+                                                      max_rb, hdr, units, err);
+  if (cudaGetLastError() != cudaSuccess) return PSW_ELAUNCH;
+  const int64_t max_items =
+      static_cast<int64_t>(n_seqs) * max_rb * L.n_kv * C::kDSplit;
+  const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
   prefill_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
       q_map, k_map, v_map, cu_q, past_lens, block_table, max_blocks, num_blocks, n_q_total,
-      max_q_len, L.n_q, L.group(), L.window, L.scale, L.softcap, out, lse, err);
+      max_q_len, L.n_q, L.group(), L.window, L.scale, L.softcap, hdr, units, out, lse, err);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 
 }  // namespace pf
 
+size_t prefill_workspace_bytes(const LayerArgs& L, int n_seqs, int max_q_len) {
+  const int T = pf::kRows / L.group();
+  const size_t max_rb = (static_cast<size_t>(max_q_len > 0 ? max_q_len : 0) + T - 1) / T;
+  const size_t bytes = sizeof(pf::PlanHeader) + static_cast<size_t>(n_seqs) * max_rb * sizeof(int2);
+  return (bytes + 255) / 256 * 256;
+}
+
 int launch_prefill(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_map,
                    const CUtensorMap& v_map, const int32_t* cu_q, const int32_t* past_lens,
                    int n_seqs, int n_q_total, int max_q_len, const int32_t* block_table,
-                   int max_blocks, int64_t num_blocks, float* out, float* lse, int32_t* err,
-                   cudaStream_t stream) {
+                   int max_blocks, int64_t num_blocks, float* out, float* lse, void* ws,
+                   int num_sms, int32_t* err, cudaStream_t stream) {
   if (L.hd == 256)
     return L.k_eq_v ? pf::launch<256, true>(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs,
                                             n_q_total, max_q_len, block_table, max_blocks,
-                                            num_blocks, out, lse, err, stream)
+                                            num_blocks, out, lse, ws, num_sms, err, stream)
                     : pf::launch<256, false>(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs,
                                              n_q_total, max_q_len, block_table, max_blocks,
-                                             num_blocks, out, lse, err, stream);
+                                             num_blocks, out, lse, ws, num_sms, err, stream);
   return L.k_eq_v ? pf::launch<512, true>(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs,
                                           n_q_total, max_q_len, block_table, max_blocks,
-                                          num_blocks, out, lse, err, stream)
+                                          num_blocks, out, lse, ws, num_sms, err, stream)
                   : pf::launch<512, false>(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs,
                                            n_q_total, max_q_len, block_table, max_blocks,
-                                           num_blocks, out, lse, err, stream);
+                                           num_blocks, out, lse, ws, num_sms, err, stream);
 }
 
 }  // namespace psw

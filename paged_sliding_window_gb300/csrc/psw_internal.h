@@ -55,12 +55,15 @@ int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse, void* ws,
                   size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream);
 
+// Prefill workspace: a work list of the (sequence, block) units.
+size_t prefill_workspace_bytes(const LayerArgs& L, int n_seqs, int max_q_len);
+
 // Returns a PSW_* code.
 int launch_prefill(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_map,
                    const CUtensorMap& v_map, const int32_t* cu_q, const int32_t* past_lens,
                    int n_seqs, int n_q_total, int max_q_len, const int32_t* block_table,
-                   int max_blocks, int64_t num_blocks, float* out, float* lse, int32_t* err,
-                   cudaStream_t stream);
+                   int max_blocks, int64_t num_blocks, float* out, float* lse, void* ws,
+                   int num_sms, int32_t* err, cudaStream_t stream);
 
 // TMA descriptor of q [n_q_total][n_q][hd] with one box = 64 columns x G
 // heads x (128 / G) tokens, 128-byte swizzle.
@@ -71,5 +74,9 @@ int make_query_tensor_map(CUtensorMap* map, const void* q, int n_q_total, int n_
 // with one box = 16 slots x 1 chunk, 128-byte swizzle.
 int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
                          int hd);
+// Pool view whose box is a whole page of box_chunks 64-element chunks of one
+// KV head, landing in shared memory as [chunk][16 rows][128 B].
+int make_pool_page_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv, int hd,
+                       int box_chunks);
 
 }  // namespace psw

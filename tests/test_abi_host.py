@@ -58,15 +58,23 @@ FULL = Layer(n_q_heads=32, n_kv_heads=4, head_dim=512, window=0, k_eq_v=True)
 
 def test_workspace_bytes_arithmetic(lib):
     # plan + (max CTAs + units) slots of 8 query heads x (head_dim floats + (m, l)) + tickets
-    def expect(layer, n_seqs):
+    # and, for prefill, a 64-byte header plus one 8-byte entry per block of
+    # 128 / G chunk tokens of every sequence; the larger of the two
+    def expect(layer, n_seqs, max_len):
         G = layer.n_q_heads // layer.n_kv_heads
         units = n_seqs * layer.n_kv_heads * ((G + 7) // 8)
         slots = 512 + units
         align = lambda x: (x + 255) // 256 * 256
-        return (align((n_seqs + 1) * 16) + align(slots * 8 * layer.head_dim * 4) +
-                align(slots * 8 * 8) + align(units * 4))
-    for layer, n in ((SLIDING, 64), (FULL, 32), (SLIDING, 0), (FULL, 1000)):
-        assert binding.workspace_bytes(layer, n, 4096) == expect(layer, n)
+        decode = (align((n_seqs + 1) * 16) + align(slots * 8 * layer.head_dim * 4) +
+                  align(slots * 8 * 8) + align(units * 4))
+        T = 128 // G
+        prefill = align(64 + n_seqs * ((max_len + T - 1) // T) * 8)
+        return max(decode, prefill)
+    for layer, n, max_len in ((SLIDING, 64, 4096), (FULL, 32, 4096), (SLIDING, 0, 4096),
+                              (FULL, 1000, 4096), (FULL, 4, 1 << 24), (SLIDING, 2, 0)):
+        assert binding.workspace_bytes(layer, n, max_len) == expect(layer, n, max_len)
+    # the prefill term dominates for few, very long sequences
+    assert expect(FULL, 4, 1 << 24) > expect(FULL, 4, 4096)
 
 
 FAKE = 0x10000  # aligned fake device address; validation never dereferences
