@@ -473,8 +473,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       int kvh, dh;
       Geom g;
       item_geom(item, kvh, dh, g);  // listed units always have rows
-      // ---- Q, once the previous item no longer needs the Q tile
+      // ---- Q, once the previous item no longer needs the Q tile (warmed in L2
+      // first, so the load that waits for it finds it there)
       if (!v_side) {
+        if (lane < C::kQChunks)
+          tma_prefetch_3d(&q_map, lane * 64, kvh * group, g.q0 + g.i0);
         if (lane == 0) {
           if (nq > 0)
             ok = mbar_wait(&bars->q_empty, (nq - 1) & 1);
@@ -728,7 +731,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           bool poly_ok = true;
           if (use_cap) {
             const float mn = min_of<BN>(x);
-            poly_ok = __all_sync(0xffffffffu, fmaxf(mx, -mn) * sc <= 0.25f);
+            // NaN (a never-cached slot beyond the sequence end, masked below)
+            // must not force the slow path: compare with "not greater"
+            poly_ok = __all_sync(0xffffffffu, !(fmaxf(mx, -mn) * sc > 0.25f));
           }
           const bool fast = interior && poly_ok;
           float tmax = 0.f;
@@ -750,13 +755,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
               for (int i = 0; i < BN / 2; ++i) z2[i] = f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), mul2);
             }
+            // columns [a, b] of the tile are visible to this row: one bit each
+            uint64_t vis = 0;
+            {
+              const int a = vis_lo - key0, b = p - key0;
+              if (row_ok && b >= 0 && a <= BN - 1) {
+                const int a0 = a < 0 ? 0 : a, b0 = b > BN - 1 ? BN - 1 : b;
+                vis = (~0ull >> (63 - b0)) & (~0ull << a0);
+              }
+            }
             float uu[BN];
 #pragma unroll
             for (int i = 0; i < BN / 2; ++i) {
               const float2 w = f2_unpack(z2[i]);
-              const int k0 = key0 + 2 * i;
-              uu[2 * i] = (row_ok && k0 >= vis_lo && k0 <= p) ? w.x : -INFINITY;
-              uu[2 * i + 1] = (row_ok && k0 + 1 >= vis_lo && k0 + 1 <= p) ? w.y : -INFINITY;
+              uu[2 * i] = (vis >> (2 * i)) & 1ull ? w.x : -INFINITY;
+              uu[2 * i + 1] = (vis >> (2 * i + 1)) & 1ull ? w.y : -INFINITY;
             }
             tmax = max_of<BN>(uu);
             if (tmax > m_run + kRescaleThreshold) {
