@@ -149,16 +149,16 @@ int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks,
 }
 
 int make_pool_page_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv, int hd,
-                       int box_chunks) {
+                       int box_slots, int box_chunks) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return PSW_ETENSORMAP;
   // [chunk of 64 elements across (kv head, head_dim)][slot][64 elements]: one
-  // box is a whole page (16 slots) of box_chunks chunks and lands in shared
-  // memory as [chunk][16 rows][128 B]
+  // box is box_slots slots (a page, or half of one) of box_chunks chunks and
+  // lands in shared memory as [chunk][box_slots rows][128 B]
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * kBlockSize,
                               static_cast<cuuint64_t>(n_kv) * (hd / 64)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n_kv) * hd * 2, 128};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockSize),
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_slots),
                              static_cast<cuuint32_t>(box_chunks)};
   const cuuint32_t estr[3] = {1, 1, 1};
   memset(map, 0, sizeof(*map));
@@ -295,12 +295,15 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
   CUtensorMap q_map, k_map, v_map;
   if ((rc = make_query_tensor_map(&q_map, q, n_q_total, L.n_q, L.hd, L.group())) != PSW_OK)
     return rc;
-  if ((rc = make_pool_tensor_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd)) != PSW_OK)
+  // K: half-page boxes over every chunk of a head ([chunk][8 rows][128 B]);
+  // V: whole-page boxes of four chunks ([chunk][16 rows][128 B])
+  if ((rc = make_pool_page_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd, kBlockSize / 2,
+                               L.hd / 64)) != PSW_OK)
     return rc;
   if (L.k_eq_v) {
     v_map = k_map;
-  } else if ((rc = make_pool_page_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd, 4)) !=
-             PSW_OK) {
+  } else if ((rc = make_pool_page_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd,
+                                      kBlockSize, 4)) != PSW_OK) {
     return rc;
   }
   return launch_prefill(L, q_map, k_map, v_map, cu_q, past_lens, n_seqs, n_q_total, max_q_len,

@@ -21,7 +21,9 @@
 //    start first and short ones fill the gaps (longest-processing-time order).
 //  * Each CTA runs warp-specialised pipelines that carry on across items:
 //    warp 8 takes the next item, loads Q (TMA, 128-byte swizzle) and streams
-//    K tiles of BN keys (64 at head_dim 256, 32 at 512) into a ring; warp 10
+//    K tiles of BN keys (64 at head_dim 256, 32 at 512) into a ring, one TMA
+//    box per 8 keys over the whole head ([group][chunk][8 rows][128 B], so the
+//    8-row groups of the K-major operand sit a fixed stride apart); warp 10
 //    streams V tiles into a second ring; both warm L2 three tiles ahead. A K
 //    stage is released once QK has read it, a V stage after PV.
 //  * Two warps issue tcgen05.mma (one elected thread each): warp 9 the QK
@@ -92,7 +94,10 @@ struct Cfg {
   static constexpr int kVChunks = kOCols / 64;
   static constexpr int kQBytes = kQChunks * kRows * 128;
   static constexpr int kChunkTileBytes = kBN * 128;  // one 64-column chunk of a K/V tile
-  static constexpr int kKBytes = kQChunks * kChunkTileBytes;
+  // K tile: [8-key group][chunk][8 rows][128 B], one TMA box per group
+  static constexpr int kKGroupBytes = kQChunks * 1024;
+  static constexpr int kKBoxes = kBN / 8;
+  static constexpr int kKBytes = kKBoxes * kKGroupBytes;
   static constexpr int kVBytes = KEQV ? 0 : kVChunks * kChunkTileBytes;
   static constexpr int kVPageBytes = kVChunks * kPageBoxBytes;  // one page of V
   static constexpr int kBarsBytes = 2432;
@@ -114,7 +119,7 @@ struct Cfg {
   static constexpr int kTmemP = 256 + 2 * kBN;  // + b * kBN; hi then lo (kBN/2 each)
   static constexpr int kTmemCols = 512;
   static_assert(kKStages >= 2, "two K stages at least");
-  static_assert(kPagesPerTile * kQChunks <= 32 && kPagesPerTile * kVChunks <= 32,
+  static_assert(kKBoxes <= 32 && kPagesPerTile <= 32,
                 "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kTmemP + 2 * kBN <= kTmemCols, "tensor memory columns");
@@ -440,8 +445,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     }
     constexpr int P = C::kPagesPerTile;
     constexpr int kTilesPerGroup = 32 / P;
-    constexpr int kKBoxes = P * C::kQChunks;
-    const int k_lp = lane / C::kQChunks, k_lc = lane - k_lp * C::kQChunks;
+    constexpr int kKBoxes = C::kKBoxes;
+    const int k_lp = lane >> 1, k_half = lane & 1;  // K: half-page box of every chunk
     const int nst = v_side ? VS : KS;
     const int my_lp = v_side ? lane : k_lp;  // V: one whole-page box per lane
     int gt = 0;  // tiles issued by this warp over all items
@@ -534,11 +539,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         __syncwarp();
         if (!v_side) {
           if (lane < kKBoxes) {
-            tma_load_3d(k_ring + stage * C::kKBytes + k_lc * C::kChunkTileBytes +
-                            k_lp * kPageBoxBytes,
-                        &k_map, full, 0, kvh * C::kQChunks + k_lc, my_blk * kBlockSize);
+            tma_load_3d(k_ring + stage * C::kKBytes + lane * C::kKGroupBytes, &k_map, full, 0,
+                        my_blk * kBlockSize + k_half * 8, kvh * C::kQChunks);
             if (jp < g.nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
-              tma_prefetch_3d(&k_map, 0, kvh * C::kQChunks + k_lc, pf_blk * kBlockSize);
+              tma_prefetch_3d(&k_map, 0, pf_blk * kBlockSize + k_half * 8, kvh * C::kQChunks);
           }
         } else {
           if (lane < P) {  // V tile: [page][chunk][16 rows][128 B]
@@ -603,15 +607,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             if (!ok) break;
             tc::fence_after();
             const uint64_t k_desc =
-                tc::smem_desc(k_base + stage * C::kKBytes, 16, 1024, tc::kSwizzle128B);
+                tc::smem_desc(k_base + stage * C::kKBytes, 16, C::kKGroupBytes, tc::kSwizzle128B);
             const uint32_t d = tmem + C::kTmemS + (g_tile & 1) * BN;
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ++ks) {
               constexpr int kQChunkBytes = kRows * 128;
               const uint32_t off_q =
                   static_cast<uint32_t>((ks >> 2) * kQChunkBytes + (ks & 3) * 32) >> 4;
-              const uint32_t off_k =
-                  static_cast<uint32_t>((ks >> 2) * C::kChunkTileBytes + (ks & 3) * 32) >> 4;
+              const uint32_t off_k = static_cast<uint32_t>((ks >> 2) * 1024 + (ks & 3) * 32) >> 4;
               tc::mma_ss(d, q_desc + off_q, k_desc + off_k, idesc_qk, ks > 0 ? 1u : 0u);
             }
             tc::commit(&bars->s_full[g_tile & 1]);
@@ -624,14 +627,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                  (!first || n == 0 || mbar_wait(&bars->o_free, (n - 1) & 1));
             if (!ok) break;
             tc::fence_after();
-            // V with k_eq_v is the K tile ([chunk][page][16 rows]); a V tile of
-            // its own is [page][chunk][16 rows]; a K16 step is one page either way
+            // V with k_eq_v is the K tile ([8-key group][chunk][8 rows]); a V
+            // tile of its own is [page][chunk][16 rows]; a K16 step is one page
+            // (two 8-key groups) either way
             const uint32_t vb = KEQV ? k_base + (g_tile % KS) * C::kKBytes +
-                                           dh * C::kVChunks * C::kChunkTileBytes
+                                           dh * C::kVChunks * 1024
                                      : v_base + (g_tile % VS) * C::kVBytes;
-            const uint64_t v_desc = tc::smem_desc(vb, KEQV ? C::kChunkTileBytes : kPageBoxBytes,
-                                                  1024, tc::kSwizzle128B);
-            constexpr int kPageStep = KEQV ? kPageBoxBytes : C::kVPageBytes;
+            const uint64_t v_desc =
+                KEQV ? tc::smem_desc(vb, 1024, C::kKGroupBytes, tc::kSwizzle128B)
+                     : tc::smem_desc(vb, kPageBoxBytes, 1024, tc::kSwizzle128B);
+            constexpr int kPageStep = KEQV ? 2 * C::kKGroupBytes : C::kVPageBytes;
             const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
@@ -807,8 +812,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           const int z_lo = max(0, g.j_lo - tkey0);       // rows [0, z_lo) hidden
           const int z_hi = min(BN, g.j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
           if (z_lo > 0 || z_hi < BN) {
-            uint8_t* vt = KEQV ? k_ring + (g_tile % KS) * C::kKBytes +
-                                     dh * C::kVChunks * C::kChunkTileBytes
+            uint8_t* vt = KEQV ? k_ring + (g_tile % KS) * C::kKBytes + dh * C::kVChunks * 1024
                                : v_ring + (g_tile % VS) * C::kVBytes;
             if (!KEQV) {  // V may land after K
               ok = __all_sync(0xffffffffu,
@@ -819,7 +823,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               const int cv = idx / (BN * 8);
               const int rem = idx - cv * (BN * 8);
               const int row = rem >> 3, uu = rem & 7;
-              const int off = KEQV ? cv * C::kChunkTileBytes + row * 128
+              const int off = KEQV ? (row >> 3) * C::kKGroupBytes + cv * 1024 + (row & 7) * 128
                                    : (row >> 4) * C::kVPageBytes + cv * kPageBoxBytes +
                                          (row & 15) * 128;
               if (row < z_lo || row >= z_hi)

@@ -74,9 +74,10 @@ int make_query_tensor_map(CUtensorMap* map, const void* q, int n_q_total, int n_
 // with one box = 16 slots x 1 chunk, 128-byte swizzle.
 int make_pool_tensor_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
                          int hd);
-// Pool view whose box is a whole page of box_chunks 64-element chunks of one
-// KV head, landing in shared memory as [chunk][16 rows][128 B].
+// Pool view whose box is box_slots slots (a page or half of one) of box_chunks
+// 64-element chunks of one KV head, landing in shared memory as
+// [chunk][box_slots rows][128 B].
 int make_pool_page_map(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv, int hd,
-                       int box_chunks);
+                       int box_slots, int box_chunks);
 
 }  // namespace psw
