@@ -37,7 +37,7 @@
 //    one thread and the softmax warps never wait for each other. The row
 //    maximum comes from the raw scores (the softcap is monotone); the softcap
 //    is an odd polynomial on the FMA pipe where every |s/cap| of the warp's
-//    tile is at most 1/2 (the exp formula elsewhere); the band/causal
+//    tile is at most 1/4 (the exp formula elsewhere); the band/causal
 //    predicate is applied on edge tiles only; the online softmax runs in fp32
 //    in the exp2 domain with lazy rescaling of O (only when the running
 //    maximum grows by more than 2^8). P is written back to tensor memory as a
@@ -274,59 +274,36 @@ __device__ __forceinline__ float tanh_p7(float y) {
   return fmaf(r * y2, y, y);
 }
 
-// z = A x + c0 + x^3 (C1 + x^2 (C2 + x^2 C3)) on N raw scores x, two per packed
-// register (without softcap C1 = C2 = C3 = 0 and only A x + c0 is formed);
-// every stage runs over 8 pairs before the next so the dependent FMAs of one
-// pair interleave with those of the others.
+// z = x (A + x^2 (C1 + x^2 (C2 + x^2 C3))) + c0 on N raw scores x, two per
+// packed register, in Horner form (without softcap C1 = C2 = C3 = 0 and only
+// A x + c0 is formed): five packed FMAs per pair.
 template <int N>
 __device__ __forceinline__ void log2_terms(const float* x, uint64_t* z2, bool cap, float A,
                                            float C1, float C2, float C3, float c0) {
-  constexpr int G = 8;
   const uint64_t A2 = f2_pack(A, A), c02 = f2_pack(c0, c0);
   const uint64_t C12 = f2_pack(C1, C1), C22 = f2_pack(C2, C2), C32 = f2_pack(C3, C3);
 #pragma unroll
-  for (int gb = 0; gb < N / 2; gb += G) {
-    uint64_t xx[G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) xx[k] = f2_pack(x[2 * (gb + k)], x[2 * (gb + k) + 1]);
+  for (int k = 0; k < N / 2; ++k) {
+    const uint64_t xx = f2_pack(x[2 * k], x[2 * k + 1]);
     if (cap) {
-      uint64_t x2[G], x3[G], r[G];
-#pragma unroll
-      for (int k = 0; k < G; ++k) x2[k] = f2_mul(xx[k], xx[k]);
-#pragma unroll
-      for (int k = 0; k < G; ++k) x3[k] = f2_mul(xx[k], x2[k]);
-#pragma unroll
-      for (int k = 0; k < G; ++k) r[k] = f2_fma(C32, x2[k], C22);
-#pragma unroll
-      for (int k = 0; k < G; ++k) r[k] = f2_fma(r[k], x2[k], C12);
-#pragma unroll
-      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], A2, c02);
-#pragma unroll
-      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(x3[k], r[k], z2[gb + k]);
+      const uint64_t xq = f2_mul(xx, xx);
+      uint64_t r = f2_fma(C32, xq, C22);
+      r = f2_fma(r, xq, C12);
+      r = f2_fma(r, xq, A2);
+      z2[k] = f2_fma(xx, r, c02);
     } else {
-#pragma unroll
-      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], A2, c02);
+      z2[k] = f2_fma(xx, A2, c02);
     }
   }
 }
 
-__device__ __forceinline__ float tanh_small(float y) {
-  const float y2 = y * y;
-  float r = -1382.f / 155925.f;
-  r = fmaf(r, y2, 62.f / 2835.f);
-  r = fmaf(r, y2, -17.f / 315.f);
-  r = fmaf(r, y2, 2.f / 15.f);
-  r = fmaf(r, y2, -1.f / 3.f);
-  return fmaf(r * y2, y, y);
-}
-
-// tanh(y) for any y: 1 - 2 / (e^{2|y|} + 1) with the sign restored, the
-// polynomial where |y| <= 1/2 (where this form loses relative precision).
-__device__ __forceinline__ float tanh_any(float y) {
-  const float ay = fabsf(y);
-  const float t = ex2_approx(-2.f * kLog2e * ay);  // e^{-2|y|}
-  const float big = copysignf(__fdividef(1.f - t, 1.f + t), y);
-  return ay <= 0.5f ? tanh_small(y) : big;
+// tanh(y) for any y as 1 - 2 / (e^{2|y|} + 1) with the sign restored. Near 0
+// its relative error grows, but its absolute error stays a few units in the
+// last place of 1, and the softcap only needs the logit cap * tanh to absolute
+// accuracy (P = exp(logit - max)).
+__device__ __forceinline__ float tanh_exp(float y) {
+  const float t = ex2_approx(-2.f * kLog2e * fabsf(y));  // e^{-2|y|}
+  return copysignf(__fdividef(1.f - t, 1.f + t), y);
 }
 
 // maximum / minimum of N values (N a multiple of 4), two 3-input chains
@@ -673,7 +650,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const float sc = use_cap ? scale / softcap : 0.f;               // y = s_raw * sc
     const float mul = use_cap ? softcap * kLog2e : scale * kLog2e;  // log2-domain factor
     const uint64_t mul2 = f2_pack(mul, mul);
-    // x-domain coefficients: A x + x^3 (C1 + x^2 (C2 + x^2 C3)) = mul tanh(x sc)
+    // x-domain coefficients: x (A + x^2 (C1 + x^2 (C2 + x^2 C3))) = mul tanh(x sc)
     // to the y^7 term (with softcap), A x = mul x without
     const float A = use_cap ? sc * mul : mul;
     const float B = sc * sc;
@@ -724,9 +701,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         // z: log2-domain exponent of P (score minus the running maximum).
         // Fast path (interior tile, every |s/cap| of the warp's tile <= 1/4):
         // the row maximum comes from the raw maximum (the softcap is monotone)
-        // and z = x A - m + x^3 r(x^2), the odd Taylor polynomial of tanh
-        // through y^7 (next term below 8.3e-8) with the scale, the softcap and
-        // log2 e folded into its coefficients: six packed FMAs per pair.
+        // and z = x r(x^2) - m, the odd Taylor polynomial of tanh through y^7
+        // (next term below 8.3e-8) with the scale, the softcap and log2 e
+        // folded into its coefficients: five packed FMAs per pair.
         // Otherwise (edge tiles, larger |s/cap|) the capped scores are formed
         // first, hidden keys are set to -inf, and their maximum is taken.
         uint64_t z2[BN / 2];
@@ -755,7 +732,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             } else if (use_cap) {
 #pragma unroll
               for (int i = 0; i < BN / 2; ++i)
-                z2[i] = f2_pack(mul * tanh_any(x[2 * i] * sc), mul * tanh_any(x[2 * i + 1] * sc));
+                z2[i] = f2_pack(mul * tanh_exp(x[2 * i] * sc), mul * tanh_exp(x[2 * i + 1] * sc));
             } else {
 #pragma unroll
               for (int i = 0; i < BN / 2; ++i) z2[i] = f2_mul(f2_pack(x[2 * i], x[2 * i + 1]), mul2);
