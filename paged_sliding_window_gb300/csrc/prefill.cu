@@ -276,23 +276,35 @@ __device__ __forceinline__ float tanh_p7(float y) {
 
 // z = x (A + x^2 (C1 + x^2 (C2 + x^2 C3))) + c0 on N raw scores x, two per
 // packed register, in Horner form (without softcap C1 = C2 = C3 = 0 and only
-// A x + c0 is formed): five packed FMAs per pair.
+// A x + c0 is formed): five packed FMAs per pair. Every Horner step runs over
+// 8 pairs before the next, so the dependent FMAs of one pair interleave with
+// those of the others.
 template <int N>
 __device__ __forceinline__ void log2_terms(const float* x, uint64_t* z2, bool cap, float A,
                                            float C1, float C2, float C3, float c0) {
+  constexpr int G = (N / 2 < 8) ? N / 2 : 8;
   const uint64_t A2 = f2_pack(A, A), c02 = f2_pack(c0, c0);
   const uint64_t C12 = f2_pack(C1, C1), C22 = f2_pack(C2, C2), C32 = f2_pack(C3, C3);
 #pragma unroll
-  for (int k = 0; k < N / 2; ++k) {
-    const uint64_t xx = f2_pack(x[2 * k], x[2 * k + 1]);
+  for (int gb = 0; gb < N / 2; gb += G) {
+    uint64_t xx[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) xx[k] = f2_pack(x[2 * (gb + k)], x[2 * (gb + k) + 1]);
     if (cap) {
-      const uint64_t xq = f2_mul(xx, xx);
-      uint64_t r = f2_fma(C32, xq, C22);
-      r = f2_fma(r, xq, C12);
-      r = f2_fma(r, xq, A2);
-      z2[k] = f2_fma(xx, r, c02);
+      uint64_t xq[G], r[G];
+#pragma unroll
+      for (int k = 0; k < G; ++k) xq[k] = f2_mul(xx[k], xx[k]);
+#pragma unroll
+      for (int k = 0; k < G; ++k) r[k] = f2_fma(C32, xq[k], C22);
+#pragma unroll
+      for (int k = 0; k < G; ++k) r[k] = f2_fma(r[k], xq[k], C12);
+#pragma unroll
+      for (int k = 0; k < G; ++k) r[k] = f2_fma(r[k], xq[k], A2);
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], r[k], c02);
     } else {
-      z2[k] = f2_fma(xx, A2, c02);
+#pragma unroll
+      for (int k = 0; k < G; ++k) z2[gb + k] = f2_fma(xx[k], A2, c02);
     }
   }
 }
