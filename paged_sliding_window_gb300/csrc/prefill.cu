@@ -27,11 +27,12 @@
 //    streams V tiles into a second ring; both warm L2 three tiles ahead. A K
 //    stage is released once QK has read it, a V stage after PV.
 //  * Two warps issue tcgen05.mma (one elected thread each): warp 9 the QK
-//    stream S_j = Q K_j^T (SS, both K-major) into one of two S buffers in
-//    tensor memory, warp 11 the PV stream O += P_j V_j (TS: P from one of two
-//    P buffers in tensor memory, V MN-major). QK of tile g + 2 runs while the
-//    softmax works on tile g; the next item's QK starts as soon as its Q has
-//    landed, while the softmax warps still finish the previous item.
+//    stream S_j = Q K_j^T (SS, both K-major) into one of four S/P buffers in
+//    tensor memory, warp 11 the PV stream O += P_j V_j (TS: P from the same
+//    buffer, where the softmax wrote it over S_j; V MN-major). QK runs up to
+//    four tiles ahead of PV, so S is ready whenever the softmax is; the next
+//    item's QK starts as soon as its Q has landed, while the softmax warps
+//    still finish the previous item.
 //  * Warps 0-3 run the softmax: warp w owns the 32 rows of tensor-memory lane
 //    quadrant w and all key columns of a tile, so row maxima and sums stay in
 //    one thread and the softmax warps never wait for each other. The row
@@ -113,25 +114,28 @@ struct Cfg {
   // swizzle atoms); checked at run time
   static constexpr int kSlack = (232448 - kUsed) < 1024 ? (232448 - kUsed) : 1024;
   static constexpr int kSmemBytes = kUsed + kSlack;
-  // tensor memory columns: O | S0 | S1 | P0 (hi, lo) | P1 (hi, lo)
+  // tensor memory columns: O | four S/P buffers
   static constexpr int kTmemO = 0;
-  static constexpr int kTmemS = 256;            // + b * kBN
-  static constexpr int kTmemP = 256 + 2 * kBN;  // + b * kBN; hi then lo (kBN/2 each)
+  // S/P buffers: S_g lands in buffer g mod kSP; the softmax reads all of it
+  // and writes P_g (bf16 hi in the first kBN/2 columns, lo in the next) over it
+  static constexpr int kSP = 4;
+  static constexpr int kTmemS = 256;  // + b * kBN
   static constexpr int kTmemCols = 512;
   static_assert(kKStages >= 2, "two K stages at least");
   static_assert(kKBoxes <= 32 && kPagesPerTile <= 32,
                 "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(kTmemP + 2 * kBN <= kTmemCols, "tensor memory columns");
+  static_assert(kTmemS + kSP * kBN <= kTmemCols, "tensor memory columns");
 };
 
 struct Bars {
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t s_full[4], p_full[4], p_free[4];
   uint64_t o_full, o_free;
   uint64_t mma_drained;
+  uint64_t v_fix;  // a V tile with hidden rows lands here before they are zeroed
   int32_t item[2];
   uint32_t tmem_base;
   int32_t abort;
@@ -277,12 +281,12 @@ __device__ __forceinline__ float tanh_p7(float y) {
 // z = x (A + x^2 (C1 + x^2 (C2 + x^2 C3))) + c0 on N raw scores x, two per
 // packed register, in Horner form (without softcap C1 = C2 = C3 = 0 and only
 // A x + c0 is formed): five packed FMAs per pair. Every Horner step runs over
-// 8 pairs before the next, so the dependent FMAs of one pair interleave with
+// 16 pairs before the next, so the dependent FMAs of one pair interleave with
 // those of the others.
 template <int N>
 __device__ __forceinline__ void log2_terms(const float* x, uint64_t* z2, bool cap, float A,
                                            float C1, float C2, float C3, float c0) {
-  constexpr int G = (N / 2 < 8) ? N / 2 : 8;
+  constexpr int G = (N / 2 < 16) ? N / 2 : 16;
   const uint64_t A2 = f2_pack(A, A), c02 = f2_pack(c0, c0);
   const uint64_t C12 = f2_pack(C1, C1), C22 = f2_pack(C2, C2), C32 = f2_pack(C3, C3);
 #pragma unroll
@@ -318,26 +322,41 @@ __device__ __forceinline__ float tanh_exp(float y) {
   return copysignf(__fdividef(1.f - t, 1.f + t), y);
 }
 
-// maximum / minimum of N values (N a multiple of 4), two 3-input chains
+// maximum / minimum of N values (N a multiple of 8), four 3-input chains
 template <int N>
 __device__ __forceinline__ float max_of(const float* x) {
-  float a = x[0], b = x[1];
+  float a = x[0], b = x[1], c = x[2], d = x[3];
 #pragma unroll
-  for (int i = 2; i + 1 < N; i += 4) {
+  for (int i = 4; i + 7 < N + 4; i += 8) {
     a = max3f(a, x[i], x[i + 1]);
-    b = (i + 3 < N) ? max3f(b, x[i + 2], x[i + 3]) : b;
+    b = max3f(b, x[i + 2], x[i + 3]);
+    if (i + 7 < N) {
+      c = max3f(c, x[i + 4], x[i + 5]);
+      d = max3f(d, x[i + 6], x[i + 7]);
+    }
   }
-  return fmaxf(a, b);
+  return fmaxf(fmaxf(a, b), fmaxf(c, d));
 }
 template <int N>
 __device__ __forceinline__ float min_of(const float* x) {
-  float a = x[0], b = x[1];
+  float a = x[0], b = x[1], c = x[2], d = x[3];
 #pragma unroll
-  for (int i = 2; i + 1 < N; i += 4) {
+  for (int i = 4; i + 7 < N + 4; i += 8) {
     a = min3f(a, x[i], x[i + 1]);
-    b = (i + 3 < N) ? min3f(b, x[i + 2], x[i + 3]) : b;
+    b = min3f(b, x[i + 2], x[i + 3]);
+    if (i + 7 < N) {
+      c = min3f(c, x[i + 4], x[i + 5]);
+      d = min3f(d, x[i + 6], x[i + 7]);
+    }
   }
-  return fminf(a, b);
+  return fminf(fminf(a, b), fminf(c, d));
+}
+
+// A whole warp waits for a phase: one non-blocking test first (the phase is
+// usually complete already), the bounded blocking wait only when it is not.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
 // ---------------------------------------------------------------- kernel
@@ -391,13 +410,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], kSoftmaxWarps);
       mbar_init(&bars->p_full[i], kSoftmaxWarps);
       mbar_init(&bars->p_free[i], 1);
+      mbar_init(&bars->s_full[i + 2], 1);
+      mbar_init(&bars->p_full[i + 2], kSoftmaxWarps);
+      mbar_init(&bars->p_free[i + 2], 1);
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, kEpiWarps);
     mbar_init(&bars->mma_drained, 2);  // one commit from each MMA thread
+    mbar_init(&bars->v_fix, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -438,8 +460,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     const int k_lp = lane >> 1, k_half = lane & 1;  // K: half-page box of every chunk
     const int nst = v_side ? VS : KS;
     const int my_lp = v_side ? lane : k_lp;  // V: one whole-page box per lane
-    int gt = 0;  // tiles issued by this warp over all items
-    int nq = 0;  // Q tiles issued
+    int gt = 0;     // tiles issued by this warp over all items
+    int nq = 0;     // Q tiles issued
+    int n_fix = 0;  // V tiles that landed on v_fix
     bool ok = true;
     for (int n = 0; ok; ++n) {
       // ---- the item: the K warp takes it and publishes it, the V warp reads it
@@ -524,7 +547,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         if (lane == 0) ok = mbar_wait(empty, ph ^ 1) && !*abort_flag;
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(full, v_side ? C::kVBytes : C::kKBytes);
+        // V rows of keys that no row of the item may see (before the window
+        // of its first row, after its last row) must not reach O: such a tile
+        // lands on v_fix first, those rows are zeroed here, and only then is
+        // v_full completed (by a plain arrival)
+        const int key0 = (g.kt0 + j) * BN;
+        const int z_lo = max(0, g.j_lo - key0);       // rows [0, z_lo) hidden
+        const int z_hi = min(BN, g.j_hi - key0 + 1);  // rows [z_hi, BN) hidden
+        const bool fix = v_side && (z_lo > 0 || z_hi < BN);
+        if (lane == 0)
+          mbar_arrive_expect_tx(fix ? &bars->v_fix : full, v_side ? C::kVBytes : C::kKBytes);
         __syncwarp();
         if (!v_side) {
           if (lane < kKBoxes) {
@@ -534,11 +566,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               tma_prefetch_3d(&k_map, 0, pf_blk * kBlockSize + k_half * 8, kvh * C::kQChunks);
           }
         } else {
+          uint8_t* vt = v_ring + stage * C::kVBytes;
           if (lane < P) {  // V tile: [page][chunk][16 rows][128 B]
             const int z = kvh * C::kQChunks + dh * C::kVChunks;
-            tma_load_3d(v_ring + stage * C::kVBytes + lane * C::kVPageBytes, &v_map, full, 0,
+            tma_load_3d(vt + lane * C::kVPageBytes, &v_map, fix ? &bars->v_fix : full, 0,
                         my_blk * kBlockSize, z);
             if (jp < g.nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, pf_blk * kBlockSize, z);
+          }
+          if (fix) {
+            if (lane == 0) ok = mbar_wait(&bars->v_fix, static_cast<uint32_t>(n_fix) & 1u);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            ++n_fix;
+            if (!ok) break;
+            for (int idx = lane; idx < BN * C::kVChunks * 8; idx += 32) {
+              const int row = idx / (C::kVChunks * 8), rem = idx - row * (C::kVChunks * 8);
+              const int cv = rem >> 3, u = rem & 7;
+              if (row < z_lo || row >= z_hi)
+                *reinterpret_cast<uint4*>(vt + (row >> 4) * C::kVPageBytes + cv * kPageBoxBytes +
+                                          (row & 15) * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // the tensor core reads these rows
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full);
           }
         }
       }
@@ -556,8 +605,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
   } else if (warp == kQkWarp || warp == kPvWarp) {
     // ------------------------------------------------------------ MMA issuers
     // Two warps issue tcgen05.mma, one elected thread each: warp kQkWarp the
-    // QK stream S_g = Q K_g^T (into S buffer g mod 2, once the softmax has read
-    // the S of tile g - 2 and K_g has landed), warp kPvWarp the PV stream
+    // QK stream S_g = Q K_g^T (into S/P buffer g mod 4, once PV has consumed
+    // the P of tile g - 4 there and K_g has landed), warp kPvWarp the PV stream
     // O += P_g V_g (once P_g is in tensor memory and V_g has landed). Each
     // stream depends only on earlier tiles, a commit tracks only its own
     // thread's MMAs, and the tensor pipe interleaves the two streams.
@@ -589,15 +638,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           }
           if (qk_side) {
             const int stage = g_tile % KS;
+            const int b = g_tile % C::kSP;  // its previous P (tile g - kSP) must be consumed
             ok = (!first || mbar_wait(&bars->q_full, n & 1)) &&
                  mbar_wait(&bars->k_full[stage], (g_tile / KS) & 1) &&
-                 (g_tile < 2 ||
-                  mbar_wait(&bars->s_free[g_tile & 1], ((g_tile >> 1) - 1) & 1));
+                 (g_tile < C::kSP ||
+                  mbar_wait(&bars->p_free[b], ((g_tile / C::kSP) - 1) & 1));
             if (!ok) break;
             tc::fence_after();
             const uint64_t k_desc =
                 tc::smem_desc(k_base + stage * C::kKBytes, 16, C::kKGroupBytes, tc::kSwizzle128B);
-            const uint32_t d = tmem + C::kTmemS + (g_tile & 1) * BN;
+            const uint32_t d = tmem + C::kTmemS + b * BN;
 #pragma unroll
             for (int ks = 0; ks < HD / 16; ++ks) {
               constexpr int kQChunkBytes = kRows * 128;
@@ -606,12 +656,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               const uint32_t off_k = static_cast<uint32_t>((ks >> 2) * 1024 + (ks & 3) * 32) >> 4;
               tc::mma_ss(d, q_desc + off_q, k_desc + off_k, idesc_qk, ks > 0 ? 1u : 0u);
             }
-            tc::commit(&bars->s_full[g_tile & 1]);
+            tc::commit(&bars->s_full[b]);
             if (!KEQV) tc::commit(&bars->k_empty[stage]);  // K read by QK
             if (last) tc::commit(&bars->q_empty);          // the Q tile may be replaced
           } else {
-            const int pb = g_tile & 1;
-            ok = mbar_wait(&bars->p_full[pb], (g_tile >> 1) & 1) &&
+            const int pb = g_tile % C::kSP;
+            ok = mbar_wait(&bars->p_full[pb], (g_tile / C::kSP) & 1) &&
                  (KEQV || mbar_wait(&bars->v_full[g_tile % VS], (g_tile / VS) & 1)) &&
                  (!first || n == 0 || mbar_wait(&bars->o_free, (n - 1) & 1));
             if (!ok) break;
@@ -626,7 +676,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 KEQV ? tc::smem_desc(vb, 1024, C::kKGroupBytes, tc::kSwizzle128B)
                      : tc::smem_desc(vb, kPageBoxBytes, 1024, tc::kSwizzle128B);
             constexpr int kPageStep = KEQV ? 2 * C::kKGroupBytes : C::kVPageBytes;
-            const uint32_t p_hi = tmem + C::kTmemP + pb * BN;
+            const uint32_t p_hi = tmem + C::kTmemS + pb * BN;
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
               const uint64_t bdesc = v_desc + static_cast<uint32_t>((ks * kPageStep) >> 4);
@@ -686,10 +736,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
       const int vis_lo = (window > 0) ? max(0, p - window + 1) : 0;  // row sees [vis_lo, p]
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < g.nkt; ++j, ++g_tile) {
-        const int sb = g_tile & 1;
+        const int sb = g_tile % C::kSP;
         // every decision below is warp-uniform
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (g_tile >> 1) & 1)) &&
-             !*abort_flag;
+        ok = warp_wait(&bars->s_full[sb], (g_tile / C::kSP) & 1) && !*abort_flag;
         if (!ok) break;
         tc::fence_after();
         float x[BN];
@@ -703,9 +752,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < BN; ++i) x[i] = __uint_as_float(v[i]);
         }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
         const int key0 = (g.kt0 + j) * BN;
         const bool interior =
@@ -780,7 +826,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         // rescaling O needs the item's previous PV finished
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           const int gprev = g_tile - 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free[gprev & 1], (gprev >> 1) & 1));
+          ok = warp_wait(&bars->p_free[gprev % C::kSP], (gprev / C::kSP) & 1);
           if (!ok) break;
           tc::fence_after();
 #pragma unroll 1
@@ -795,36 +841,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           }
           tc::wait_st();
         }
-        // zero V rows that no row of this item can see (its first / last key tile)
-        if (j == 0 || j == g.nkt - 1) {
+        // with k_eq_v, V is this tile's K stage (landed: S was formed from it;
+        // not reloaded before PV has read it): zero the rows of keys that no
+        // row of the item may see on its first / last tile. A V tile of its
+        // own is zeroed by the V producer before it is reported.
+        if (KEQV && (j == 0 || j == g.nkt - 1)) {
           const int tkey0 = (g.kt0 + j) * BN;
           const int z_lo = max(0, g.j_lo - tkey0);       // rows [0, z_lo) hidden
           const int z_hi = min(BN, g.j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
           if (z_lo > 0 || z_hi < BN) {
-            uint8_t* vt = KEQV ? k_ring + (g_tile % KS) * C::kKBytes + dh * C::kVChunks * 1024
-                               : v_ring + (g_tile % VS) * C::kVBytes;
-            if (!KEQV) {  // V may land after K
-              ok = __all_sync(0xffffffffu,
-                              mbar_wait(&bars->v_full[g_tile % VS], (g_tile / VS) & 1));
-              if (!ok) break;
-            }
+            uint8_t* vt = k_ring + (g_tile % KS) * C::kKBytes + dh * C::kVChunks * 1024;
             for (int idx = threadIdx.x; idx < C::kVChunks * BN * 8; idx += kSoftmaxWarps * 32) {
               const int cv = idx / (BN * 8);
               const int rem = idx - cv * (BN * 8);
               const int row = rem >> 3, uu = rem & 7;
-              const int off = KEQV ? (row >> 3) * C::kKGroupBytes + cv * 1024 + (row & 7) * 128
-                                   : (row >> 4) * C::kVPageBytes + cv * kPageBoxBytes +
-                                         (row & 15) * 128;
+              const int off = (row >> 3) * C::kKGroupBytes + cv * 1024 + (row & 7) * 128;
               if (row < z_lo || row >= z_hi)
                 *reinterpret_cast<uint4*>(vt + off + uu * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
           }
-        }
-        // P_{g-2} must have been multiplied in before its buffer is rewritten
-        if (g_tile >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_free[sb], ((g_tile >> 1) - 1) & 1));
-          if (!ok) break;
         }
         {
           // P = 2^z: bf16 high part and bf16 remainder into tensor memory, 16
@@ -860,7 +896,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                 lo[gb + k] = __byte_perm(__float_as_uint(l.x), __float_as_uint(l.y), 0x7632);
               }
             }
-            const uint32_t pcol = tmem + lane_off + C::kTmemP + sb * BN + c * kChunkPairs;
+            const uint32_t pcol = tmem + lane_off + C::kTmemS + sb * BN + c * kChunkPairs;
             if constexpr (kChunkPairs == 16) {
               tc::st16(pcol, hi);
               tc::st16(pcol + BN / 2, lo);
