@@ -40,9 +40,10 @@
 //    is an odd polynomial on the FMA pipe where every |s/cap| of the warp's
 //    tile is at most 1/4 (the exp formula elsewhere); the band/causal
 //    predicate is applied on edge tiles only; the online softmax runs in fp32
-//    in the exp2 domain with lazy rescaling of O (only when the running
-//    maximum grows by more than 2^8). P is written back to tensor memory as a
-//    bf16 high part and a bf16 remainder (integer ops, no conversions); both
+//    in the exp2 domain with a running maximum first set a factor 2^64
+//    above the largest score seen and raised (O rescaled) only when a score
+//    exceeds it by another 2^64 (rescales are rare). P is written back to tensor
+//    memory as a bf16 high part and a bf16 remainder (integer ops); both
 //    are multiplied into O, so P enters the product to 2^-14 relative.
 //  * Warps 4-7 are the epilogue: once an item's last PV is done they scale
 //    its O by 1/l, stage it per warp through shared memory 32 columns at a
@@ -73,7 +74,20 @@ constexpr int kRows = 128;
 constexpr int kPageBoxBytes = kBlockSize * 128;  // one TMA box: 16 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.f;  // log2 units
+// Running maximum m of a row (log2 units). When a row's first visible keys
+// arrive, m is set kMaxBias above their largest score; afterwards it is raised
+// (and O rescaled by 2^(m_old - m_new)) only once a score exceeds it by more
+// than kRescaleThreshold, and then to that score. So P = 2^(z - m) <= 2^64,
+// l < 2^95 for up to 2^31 keys and O stays below the fp32 limit while
+// |V| < 2^33. Keys more than 62 below the row's first maximum flush to zero
+// (below 2^-62 of that key). The rescale factor underflows only when the old
+// terms, at most 2^64 before it, fall below 2^-62 of the new maximum key.
+// Rescales of O wait for the previous PV, so they should be rare: a row's
+// maximum must grow by 128 after its first visible keys (a row whose first
+// tile holds few of its keys would otherwise rescale on its second tile,
+// while the accumulator may still be held by the previous item's epilogue).
+constexpr float kRescaleThreshold = 64.f;
+constexpr float kMaxBias = 64.f;
 constexpr int kCostBuckets = 4096;       // plan: units sorted by tile count (capped)
 constexpr int kPlanThreads = 1024;
 
@@ -780,8 +794,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           if (fast) tmax = use_cap ? mul * tanh_p7(mx * sc) : mx * mul;
           if (fast) {
             if (tmax > m_run + kRescaleThreshold) {  // lazy rescale (also the first key)
-              alpha = ex2_approx(m_run - tmax);
-              m_run = tmax;
+              // first visible keys of the row: O = 0, nothing to rescale
+              alpha = (m_run == -INFINITY) ? 1.f : ex2_approx(m_run - tmax);
+              m_run = (m_run == -INFINITY) ? tmax + kMaxBias : tmax;
             }
             log2_terms<BN>(x, z2, use_cap, A, C1, C2, C3, -m_run);
           } else {
@@ -813,8 +828,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             }
             tmax = max_of<BN>(uu);
             if (tmax > m_run + kRescaleThreshold) {
-              alpha = ex2_approx(m_run - tmax);
-              m_run = tmax;
+              alpha = (m_run == -INFINITY) ? 1.f : ex2_approx(m_run - tmax);
+              m_run = (m_run == -INFINITY) ? tmax + kMaxBias : tmax;
             }
             const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
             const uint64_t negm2 = f2_pack(-m_use, -m_use);
@@ -977,15 +992,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         lse[static_cast<int64_t>(g.q0 + g.i0 + t) * n_q + kvh * group + h] =
             (l_row > 0.f) ? (m_row + log2f(l_row)) * kLn2 : -INFINITY;
       tc::fence_after();
+      // two 32-column blocks (four loads) in flight per wait
 #pragma unroll 1
-      for (int cb = 0; cb < C::kOCols / 32; ++cb) {
+      for (int cb = 0; cb < C::kOCols / 32; cb += 2) {
+        uint32_t v[4][16];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v[16];
-          tc::ld16x256_x4(tmem + (static_cast<uint32_t>(quad * 32 + hf * 16) << 16) +
-                              C::kTmemO + cb * 32,
-                          v);
-          tc::wait_ld();
+        for (int q = 0; q < 4; ++q)
+          tc::ld16x256_x4(tmem + (static_cast<uint32_t>(quad * 32 + (q & 1) * 16) << 16) +
+                              C::kTmemO + (cb + (q >> 1)) * 32,
+                          v[q]);
+        tc::wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int hf = q & 1, cc = cb + (q >> 1);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -993,9 +1012,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               const int e = hf * 2 + e2;
               if (valid[e]) {
                 float2 w;
-                w.x = __uint_as_float(v[4 * k + 2 * e2]) * inv[e];
-                w.y = __uint_as_float(v[4 * k + 2 * e2 + 1]) * inv[e];
-                *reinterpret_cast<float2*>(orow[e] + cb * 32 + 8 * k) = w;
+                w.x = __uint_as_float(v[q][4 * k + 2 * e2]) * inv[e];
+                w.y = __uint_as_float(v[q][4 * k + 2 * e2 + 1]) * inv[e];
+                *reinterpret_cast<float2*>(orow[e] + cc * 32 + 8 * k) = w;
               }
             }
           }

@@ -122,3 +122,57 @@ def test_prefill_invalid_block_is_flagged():
     g.pages = binding.make_pages(bad, step.cache.num_blocks)
     g.prefill()
     assert binding.get_error() & binding.DEVERR_BLOCK_ID
+
+
+def _crafted_scores(step, row, key_pos_to_dim0):
+    """Query `row`, head 0 = 16 e_0 (RMS 1) and keys of KV head 0 = c e_0, so
+    that the scale-1 score of key j is 16 c_j exactly (all values bf16)."""
+    q = np.zeros(step.layer.head_dim, np.float32)
+    q[0] = 16.0
+    step.q[row, 0] = wl.f32_to_bf16_bits(q)
+    past = int(step.past_lens[0])
+    c = step.cache
+    for j, cj in key_pos_to_dim0.items():
+        k = np.zeros(step.layer.head_dim, np.float32)
+        k[0] = cj
+        bits = wl.f32_to_bf16_bits(k)
+        if j >= past:
+            step.new_k[int(step.cu_new[0]) + j - past, 0] = bits
+        else:
+            step.cache.hist_k[int(c.hist_cu[0]) + j - int(c.hist_past[0]), 0] = bits
+
+
+def _low_first_then_growth():
+    """Keys 0-63 score -100, keys 64-127 score -12, key 128 scores -10 and keys
+    129-130 score -100 for the query at position 130: the row's maximum grows
+    by about 130 (log2 units) in two steps, and the second step's tile carries
+    90 % of the weight."""
+    keys = {j: -6.25 for j in range(64)}
+    keys.update({j: -0.75 for j in range(64, 128)})
+    keys.update({128: -0.625, 129: -6.25, 130: -6.25})
+    return keys
+
+
+def test_prefill_rescale_after_low_first_maximum(orc):
+    """A row whose first key tile holds only very low scores, then a tile far
+    above them, then a slightly higher key: the running maximum is raised
+    twice and the earlier tiles must keep their weight through the rescale."""
+    layer = Layer(4, 4, 256, window=0, scale=1.0)
+    step = wl.custom_step(layer, 61, [0], [192])
+    _crafted_scores(step, 130, _low_first_then_growth())
+    run_prefill(orc, step)
+
+
+def test_decode_rescale_after_low_first_maximum(orc):
+    """The same scores seen by a decode query at position 130."""
+    layer = Layer(4, 4, 256, window=0, scale=1.0)
+    step = wl.custom_step(layer, 62, [130], [1])
+    _crafted_scores(step, 0, _low_first_then_growth())
+    g = GpuStep(step)
+    g.write_new()
+    g.decode()
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    ref_out, ref_lse = OracleStep(orc, step).decode()
+    assert_close(g.out.cpu().numpy(), ref_out, "decode out")
+    assert_close(g.lse.cpu().numpy(), ref_lse, "decode lse")
