@@ -295,10 +295,12 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
   CUtensorMap q_map, k_map, v_map;
   if ((rc = make_query_tensor_map(&q_map, q, n_q_total, L.n_q, L.hd, L.group())) != PSW_OK)
     return rc;
-  // K: half-page boxes over every chunk of a head ([chunk][8 rows][128 B]);
+  // K: half-page boxes over every chunk of a head ([chunk][8 rows][128 B]),
+  // or over one head_dim half at head_dim 512 with k_eq_v;
   // V: whole-page boxes of four chunks ([chunk][16 rows][128 B])
+  const int k_box_chunks = (L.hd == 512 && L.k_eq_v) ? 4 : L.hd / 64;
   if ((rc = make_pool_page_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd, kBlockSize / 2,
-                               L.hd / 64)) != PSW_OK)
+                               k_box_chunks)) != PSW_OK)
     return rc;
   if (L.k_eq_v) {
     v_map = k_map;

@@ -102,15 +102,23 @@ static_assert(sizeof(PlanHeader) == 64, "plan header");
 template <int HD, bool KEQV>
 struct Cfg {
   static constexpr int kQChunks = HD / 64;
-  static constexpr int kBN = (HD == 256) ? 64 : 32;
+  // head_dim 512 with k_eq_v: 64-key tiles loaded as two stages of one
+  // head_dim half each, the half that is not this item's V first; it is
+  // released once QK has read it, the item's own half (its V) after PV. The
+  // 128 KB Q tile is then read by the QK MMAs once per 64 keys, not per 32.
+  static constexpr bool kSplitK = (HD == 512) && KEQV;
+  static constexpr int kKHalves = kSplitK ? 2 : 1;  // K stages per tile
+  static constexpr int kBN = (HD == 256 || kSplitK) ? 64 : 32;
   static constexpr int kPagesPerTile = kBN / kBlockSize;
   static constexpr int kOCols = 256;
   static constexpr int kDSplit = HD / kOCols;
   static constexpr int kVChunks = kOCols / 64;
   static constexpr int kQBytes = kQChunks * kRows * 128;
   static constexpr int kChunkTileBytes = kBN * 128;  // one 64-column chunk of a K/V tile
-  // K tile: [8-key group][chunk][8 rows][128 B], one TMA box per group
-  static constexpr int kKGroupBytes = kQChunks * 1024;
+  // K stage: [8-key group][chunk][8 rows][128 B], one TMA box per group (all
+  // chunks of the head, or the chunks of one head_dim half with kSplitK)
+  static constexpr int kKBoxChunks = kQChunks / kKHalves;
+  static constexpr int kKGroupBytes = kKBoxChunks * 1024;
   static constexpr int kKBoxes = kBN / 8;
   static constexpr int kKBytes = kKBoxes * kKGroupBytes;
   static constexpr int kVBytes = KEQV ? 0 : kVChunks * kChunkTileBytes;
@@ -135,7 +143,7 @@ struct Cfg {
   static constexpr int kSP = 4;
   static constexpr int kTmemS = 256;  // + b * kBN
   static constexpr int kTmemCols = 512;
-  static_assert(kKStages >= 2, "two K stages at least");
+  static_assert(kKStages >= 2 * kKHalves - (kSplitK ? 1 : 0), "K stages");
   static_assert(kKBoxes <= 32 && kPagesPerTile <= 32,
                 "one TMA box per producer lane");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -542,9 +550,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         return blk;
       };
       int ids = load_group(0), ids_next = load_group(1);
-      for (int j = 0; j < g.nkt; ++j, ++gt) {
-        const int stage = gt % nst;
-        const uint32_t ph = static_cast<uint32_t>(gt / nst) & 1u;
+      for (int j = 0; j < g.nkt && ok; ++j) {
         if (j > 0 && j % kTilesPerGroup == 0) {
           ids = ids_next;
           ids_next = load_group(j / kTilesPerGroup + 1);
@@ -556,11 +562,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         const int pf_same = __shfl_sync(0xffffffffu, ids, psrc);
         const int pf_next = __shfl_sync(0xffffffffu, ids_next, psrc);
         const int pf_blk = (jp / kTilesPerGroup == j / kTilesPerGroup) ? pf_same : pf_next;
-        uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
-        uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
-        if (lane == 0) ok = mbar_wait(empty, ph ^ 1) && !*abort_flag;
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
         // V rows of keys that no row of the item may see (before the window
         // of its first row, after its last row) must not reach O: such a tile
         // lands on v_fix first, those rows are zeroed here, and only then is
@@ -569,39 +570,53 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         const int z_lo = max(0, g.j_lo - key0);       // rows [0, z_lo) hidden
         const int z_hi = min(BN, g.j_hi - key0 + 1);  // rows [z_hi, BN) hidden
         const bool fix = v_side && (z_lo > 0 || z_hi < BN);
-        if (lane == 0)
-          mbar_arrive_expect_tx(fix ? &bars->v_fix : full, v_side ? C::kVBytes : C::kKBytes);
-        __syncwarp();
-        if (!v_side) {
-          if (lane < kKBoxes) {
-            tma_load_3d(k_ring + stage * C::kKBytes + lane * C::kKGroupBytes, &k_map, full, 0,
-                        my_blk * kBlockSize + k_half * 8, kvh * C::kQChunks);
-            if (jp < g.nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
-              tma_prefetch_3d(&k_map, 0, pf_blk * kBlockSize + k_half * 8, kvh * C::kQChunks);
-          }
-        } else {
-          uint8_t* vt = v_ring + stage * C::kVBytes;
-          if (lane < P) {  // V tile: [page][chunk][16 rows][128 B]
-            const int z = kvh * C::kQChunks + dh * C::kVChunks;
-            tma_load_3d(vt + lane * C::kVPageBytes, &v_map, fix ? &bars->v_fix : full, 0,
-                        my_blk * kBlockSize, z);
-            if (jp < g.nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, pf_blk * kBlockSize, z);
-          }
-          if (fix) {
-            if (lane == 0) ok = mbar_wait(&bars->v_fix, static_cast<uint32_t>(n_fix) & 1u);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            ++n_fix;
-            if (!ok) break;
-            for (int idx = lane; idx < BN * C::kVChunks * 8; idx += 32) {
-              const int row = idx / (C::kVChunks * 8), rem = idx - row * (C::kVChunks * 8);
-              const int cv = rem >> 3, u = rem & 7;
-              if (row < z_lo || row >= z_hi)
-                *reinterpret_cast<uint4*>(vt + (row >> 4) * C::kVPageBytes + cv * kPageBoxBytes +
-                                          (row & 15) * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+        const int n_st = v_side ? 1 : C::kKHalves;  // stages of this tile
+        for (int hh = 0; hh < n_st; ++hh, ++gt) {
+          const int stage = gt % nst;
+          const uint32_t ph = static_cast<uint32_t>(gt / nst) & 1u;
+          uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
+          uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
+          if (lane == 0) ok = mbar_wait(empty, ph ^ 1) && !*abort_flag;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          if (lane == 0)
+            mbar_arrive_expect_tx(fix ? &bars->v_fix : full, v_side ? C::kVBytes : C::kKBytes);
+          __syncwarp();
+          if (!v_side) {
+            // with kSplitK: head_dim half 1 - dh first (QK only), then half dh
+            const int h = C::kSplitK ? (hh == 0 ? 1 - dh : dh) : 0;
+            const int zc = kvh * C::kQChunks + h * C::kKBoxChunks;
+            if (lane < kKBoxes) {
+              tma_load_3d(k_ring + stage * C::kKBytes + lane * C::kKGroupBytes, &k_map, full, 0,
+                          my_blk * kBlockSize + k_half * 8, zc);
+              if (jp < g.nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
+                tma_prefetch_3d(&k_map, 0, pf_blk * kBlockSize + k_half * 8, zc);
             }
-            fence_proxy_async_smem();  // the tensor core reads these rows
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full);
+          } else {
+            uint8_t* vt = v_ring + stage * C::kVBytes;
+            if (lane < P) {  // V tile: [page][chunk][16 rows][128 B]
+              const int z = kvh * C::kQChunks + dh * C::kVChunks;
+              tma_load_3d(vt + lane * C::kVPageBytes, &v_map, fix ? &bars->v_fix : full, 0,
+                          my_blk * kBlockSize, z);
+              if (jp < g.nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, pf_blk * kBlockSize, z);
+            }
+            if (fix) {
+              if (lane == 0) ok = mbar_wait(&bars->v_fix, static_cast<uint32_t>(n_fix) & 1u);
+              ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+              ++n_fix;
+              if (!ok) break;
+              for (int idx = lane; idx < BN * C::kVChunks * 8; idx += 32) {
+                const int row = idx / (C::kVChunks * 8), rem = idx - row * (C::kVChunks * 8);
+                const int cv = rem >> 3, u = rem & 7;
+                if (row < z_lo || row >= z_hi)
+                  *reinterpret_cast<uint4*>(vt + (row >> 4) * C::kVPageBytes +
+                                            cv * kPageBoxBytes + (row & 15) * 128 + u * 16) =
+                      make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();  // the tensor core reads these rows
+              __syncwarp();
+              if (lane == 0) mbar_arrive(full);
+            }
           }
         }
       }
@@ -651,28 +666,41 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             break;
           }
           if (qk_side) {
-            const int stage = g_tile % KS;
             const int b = g_tile % C::kSP;  // its previous P (tile g - kSP) must be consumed
             ok = (!first || mbar_wait(&bars->q_full, n & 1)) &&
-                 mbar_wait(&bars->k_full[stage], (g_tile / KS) & 1) &&
                  (g_tile < C::kSP ||
                   mbar_wait(&bars->p_free[b], ((g_tile / C::kSP) - 1) & 1));
             if (!ok) break;
-            tc::fence_after();
-            const uint64_t k_desc =
-                tc::smem_desc(k_base + stage * C::kKBytes, 16, C::kKGroupBytes, tc::kSwizzle128B);
             const uint32_t d = tmem + C::kTmemS + b * BN;
+            constexpr int kSteps = HD / 16 / C::kKHalves;  // K16 steps per K stage
+            constexpr int kQChunkBytes = kRows * 128;
 #pragma unroll
-            for (int ks = 0; ks < HD / 16; ++ks) {
-              constexpr int kQChunkBytes = kRows * 128;
-              const uint32_t off_q =
-                  static_cast<uint32_t>((ks >> 2) * kQChunkBytes + (ks & 3) * 32) >> 4;
-              const uint32_t off_k = static_cast<uint32_t>((ks >> 2) * 1024 + (ks & 3) * 32) >> 4;
-              tc::mma_ss(d, q_desc + off_q, k_desc + off_k, idesc_qk, ks > 0 ? 1u : 0u);
+            for (int hh = 0; hh < C::kKHalves; ++hh) {
+              const int hc = g_tile * C::kKHalves + hh;  // K stage counter
+              const int stage = hc % KS;
+              ok = mbar_wait(&bars->k_full[stage], (hc / KS) & 1);
+              if (!ok) break;
+              tc::fence_after();
+              // head_dim half held by this stage (kSplitK: 1 - dh, then dh)
+              const int h = C::kSplitK ? (hh == 0 ? 1 - dh : dh) : 0;
+              const uint64_t k_desc =
+                  tc::smem_desc(k_base + stage * C::kKBytes, 16, C::kKGroupBytes, tc::kSwizzle128B);
+#pragma unroll
+              for (int kk = 0; kk < kSteps; ++kk) {
+                const int ks = h * kSteps + kk;  // K16 step over head_dim
+                const uint32_t off_q =
+                    static_cast<uint32_t>((ks >> 2) * kQChunkBytes + (ks & 3) * 32) >> 4;
+                const uint32_t off_k =
+                    static_cast<uint32_t>((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+                tc::mma_ss(d, q_desc + off_q, k_desc + off_k, idesc_qk,
+                           (hh > 0 || kk > 0) ? 1u : 0u);
+              }
+              // K read by QK (with kSplitK: the half that is not this item's V)
+              if (!KEQV || (C::kSplitK && hh == 0)) tc::commit(&bars->k_empty[stage]);
             }
+            if (!ok) break;
             tc::commit(&bars->s_full[b]);
-            if (!KEQV) tc::commit(&bars->k_empty[stage]);  // K read by QK
-            if (last) tc::commit(&bars->q_empty);          // the Q tile may be replaced
+            if (last) tc::commit(&bars->q_empty);  // the Q tile may be replaced
           } else {
             const int pb = g_tile % C::kSP;
             ok = mbar_wait(&bars->p_full[pb], (g_tile / C::kSP) & 1) &&
@@ -683,8 +711,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             // V with k_eq_v is the K tile ([8-key group][chunk][8 rows]); a V
             // tile of its own is [page][chunk][16 rows]; a K16 step is one page
             // (two 8-key groups) either way
-            const uint32_t vb = KEQV ? k_base + (g_tile % KS) * C::kKBytes +
-                                           dh * C::kVChunks * 1024
+            // with k_eq_v the K stage holding head_dim half dh (kSplitK: the
+            // tile's second stage)
+            const int vstage = (g_tile * C::kKHalves + C::kKHalves - 1) % KS;
+            const uint32_t vb = KEQV ? k_base + vstage * C::kKBytes +
+                                           (C::kSplitK ? 0 : dh * C::kVChunks * 1024)
                                      : v_base + (g_tile % VS) * C::kVBytes;
             const uint64_t v_desc =
                 KEQV ? tc::smem_desc(vb, 1024, C::kKGroupBytes, tc::kSwizzle128B)
@@ -700,7 +731,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             }
             tc::commit(&bars->p_free[pb]);
             // V (or, with k_eq_v, the whole K stage) is free once PV ends
-            tc::commit(KEQV ? &bars->k_empty[g_tile % KS] : &bars->v_empty[g_tile % VS]);
+            tc::commit(KEQV ? &bars->k_empty[vstage] : &bars->v_empty[g_tile % VS]);
             if (last) tc::commit(&bars->o_full);  // the item's O is final
           }
         }
@@ -865,7 +896,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           const int z_lo = max(0, g.j_lo - tkey0);       // rows [0, z_lo) hidden
           const int z_hi = min(BN, g.j_hi - tkey0 + 1);  // rows [z_hi, BN) hidden
           if (z_lo > 0 || z_hi < BN) {
-            uint8_t* vt = k_ring + (g_tile % KS) * C::kKBytes + dh * C::kVChunks * 1024;
+            const int vstage = (g_tile * C::kKHalves + C::kKHalves - 1) % KS;
+            uint8_t* vt = k_ring + vstage * C::kKBytes + (C::kSplitK ? 0 : dh * C::kVChunks * 1024);
             for (int idx = threadIdx.x; idx < C::kVChunks * BN * 8; idx += kSoftmaxWarps * 32) {
               const int cv = idx / (BN * 8);
               const int rem = idx - cv * (BN * 8);

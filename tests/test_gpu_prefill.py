@@ -78,6 +78,8 @@ PREFILL_CASES = [
     pytest.param(Layer(32, 4, 512, window=0, k_eq_v=True), [0, 100, 1500], [48, 17, 200],
                  id="hd512-g8-keqv"),
     pytest.param(Layer(8, 2, 512, window=48), [0, 30, 400], [100, 3, 60], id="hd512-g4-w48"),
+    pytest.param(Layer(16, 2, 512, window=100, k_eq_v=True, softcap=30.0), [0, 300, 1000],
+                 [130, 64, 70], id="hd512-g8-w100-keqv-cap"),
     pytest.param(Layer(4, 4, 256, window=0, k_eq_v=True), [0, 31], [31, 66], id="hd256-g1-keqv"),
     pytest.param(Layer(12, 4, 256, window=33), [0, 50], [45, 20], id="hd256-g3-w33"),
 ]
