@@ -21,11 +21,12 @@
 //    start first and short ones fill the gaps (longest-processing-time order).
 //  * Each CTA runs warp-specialised pipelines that carry on across items:
 //    warp 8 takes the next item, loads Q (TMA, 128-byte swizzle) and streams
-//    K tiles of BN keys (64 at head_dim 256, 32 at 512) into a ring, one TMA
-//    box per 8 keys over the whole head ([group][chunk][8 rows][128 B], so the
+//    K tiles of BN keys (64, or 32 at head_dim 512 without k_eq_v) into a
+//    ring, one TMA box per 8 keys over the whole head, or over one head_dim
+//    half at head_dim 512 with k_eq_v ([group][chunk][8 rows][128 B], so the
 //    8-row groups of the K-major operand sit a fixed stride apart); warp 10
-//    streams V tiles into a second ring; both warm L2 three tiles ahead. A K
-//    stage is released once QK has read it, a V stage after PV.
+//    streams V tiles into a second ring. A K stage is released once QK has
+//    read it (with k_eq_v: the stage holding V after PV), a V stage after PV.
 //  * Two warps issue tcgen05.mma (one elected thread each): warp 9 the QK
 //    stream S_j = Q K_j^T (SS, both K-major) into one of four S/P buffers in
 //    tensor memory, warp 11 the PV stream O += P_j V_j (TS: P from the same
@@ -557,11 +558,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         }
         const int src = (j % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
         const int my_blk = __shfl_sync(0xffffffffu, ids, src);
-        const int jp = j + 3;  // tile whose pages are warmed in L2 now
-        const int psrc = (jp % kTilesPerGroup) * P + (my_lp < P ? my_lp : 0);
-        const int pf_same = __shfl_sync(0xffffffffu, ids, psrc);
-        const int pf_next = __shfl_sync(0xffffffffu, ids_next, psrc);
-        const int pf_blk = (jp / kTilesPerGroup == j / kTilesPerGroup) ? pf_same : pf_next;
         // V rows of keys that no row of the item may see (before the window
         // of its first row, after its last row) must not reach O: such a tile
         // lands on v_fix first, those rows are zeroed here, and only then is
@@ -589,8 +585,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
             if (lane < kKBoxes) {
               tma_load_3d(k_ring + stage * C::kKBytes + lane * C::kKGroupBytes, &k_map, full, 0,
                           my_blk * kBlockSize + k_half * 8, zc);
-              if (jp < g.nkt && pf_blk >= 0)  // warm L2 with the tile three ahead
-                tma_prefetch_3d(&k_map, 0, pf_blk * kBlockSize + k_half * 8, zc);
             }
           } else {
             uint8_t* vt = v_ring + stage * C::kVBytes;
@@ -598,7 +592,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
               const int z = kvh * C::kQChunks + dh * C::kVChunks;
               tma_load_3d(vt + lane * C::kVPageBytes, &v_map, fix ? &bars->v_fix : full, 0,
                           my_blk * kBlockSize, z);
-              if (jp < g.nkt && pf_blk >= 0) tma_prefetch_3d(&v_map, 0, pf_blk * kBlockSize, z);
             }
             if (fix) {
               if (lane == 0) ok = mbar_wait(&bars->v_fix, static_cast<uint32_t>(n_fix) & 1u);
