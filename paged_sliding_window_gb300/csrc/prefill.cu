@@ -995,6 +995,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
            __all_sync(0xffffffffu, mbar_wait(&bars->stats_full[slot], (n >> 1) & 1)) &&
            !*abort_flag;
       if (!ok) break;
+      // Is this the CTA's last item? Its K producer published the next item
+      // (or the end mark) before it loaded this item's last tile.
+      const int nslot = (n + 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->item_full[nslot], ((n + 1) >> 1) & 1));
+      if (!ok) break;
+      const bool last_item = bars->item[nslot] < 0;
       // this lane's own row (lse) and the four rows it stores (two per half)
       const float m_row = bars->stat_m[slot][r];
       const float l_row = bars->stat_l[slot][r];
@@ -1017,9 +1023,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         lse[static_cast<int64_t>(g.q0 + g.i0 + t) * n_q + kvh * group + h] =
             (l_row > 0.f) ? (m_row + log2f(l_row)) * kLn2 : -INFINITY;
       tc::fence_after();
+      if (last_item) {
+        // Nothing follows this item: its last PV has completed, so every MMA
+        // and TMA copy of the CTA has, and the Q/K/V rings are free. Each
+        // thread stages its own row, scaled by 1/l, in shared memory (rows
+        // 1040 B apart, so a warp's 16-byte stores fall in distinct banks)
+        // and writes it with one bulk copy.
+        constexpr int kRowStride = C::kOCols * 4 + 16;
+        static_assert(kRows * kRowStride <= C::kQBytes + KS * C::kKBytes +
+                                                 C::kVStages * C::kVBytes,
+                      "staged output fits the rings");
+        uint8_t* srow = smem + r * kRowStride;
+        const float inv_r = (l_row > 0.f) ? 1.f / l_row : 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::kOCols; c0 += 32) {
+          uint32_t v[32];
+          tc::ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kTmemO + c0, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 w;
+            w.x = __uint_as_float(v[4 * q4]) * inv_r;
+            w.y = __uint_as_float(v[4 * q4 + 1]) * inv_r;
+            w.z = __uint_as_float(v[4 * q4 + 2]) * inv_r;
+            w.w = __uint_as_float(v[4 * q4 + 3]) * inv_r;
+            *reinterpret_cast<float4*>(srow + (c0 + 4 * q4) * 4) = w;
+          }
+        }
+        if (t < g.tok_valid) {
+          fence_proxy_async_smem();  // the bulk copy reads these rows
+          bulk_store(out + (static_cast<int64_t>(g.q0 + g.i0 + t) * n_q + kvh * group + h) * HD +
+                         dh * C::kOCols,
+                     srow, C::kOCols * 4);
+          bulk_commit();
+          bulk_wait_read();
+        }
+      }
       // two 32-column blocks (four loads) in flight per wait
 #pragma unroll 1
-      for (int cb = 0; cb < C::kOCols / 32; cb += 2) {
+      for (int cb = 0; cb < C::kOCols / 32 && !last_item; cb += 2) {
         uint32_t v[4][16];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
