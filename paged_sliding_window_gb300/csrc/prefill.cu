@@ -292,6 +292,21 @@ prefill_plan_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict_
   if (tid == 0) hdr->next_item = 0;
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from shared to global memory, tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk copy of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- softcap
 // tanh(y) for |y| <= 1/4: the odd Taylor polynomial through y^7; the first
 // omitted term, 62/2835 y^9, is below 8.3e-8 there.

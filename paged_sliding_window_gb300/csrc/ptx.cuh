@@ -137,21 +137,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// from shared to global memory, tracked by this thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until every committed bulk copy of this thread has read its source.
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tensor core) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
