@@ -484,6 +484,53 @@ def ncu_case(which):
     print(f"ncu case {which} done")
 
 
+def packed_step_io(step: wl.Step, g, device="cuda"):
+    """One pinned host buffer with every input of a decode step (q, new K and
+    V, offsets, past and sequence lengths, block table) and one device buffer
+    it is copied into, whose 256-byte-aligned pieces replace the step's device
+    tensors; likewise one device buffer holding out and lse and its pinned host
+    copy. A step then moves its inputs and its result with one transfer each."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+
+    def layout(arrays):
+        offs, off = [], 0
+        for a in arrays:
+            offs.append(off)
+            off += (a.nbytes + 255) // 256 * 256
+        return offs, off
+
+    inputs = [np.ascontiguousarray(a) for a in (
+        step.q, step.new_k, step.new_v, step.cu_new.astype(np.int32),
+        step.past_lens.astype(np.int32), step.seq_lens.astype(np.int32),
+        step.block_table.astype(np.int32))]
+    offs, n_in = layout(inputs)
+    h_in = torch.zeros(n_in, dtype=torch.uint8).pin_memory()
+    for a, o in zip(inputs, offs):
+        h_in[o:o + a.nbytes] = torch.from_numpy(a.view(np.uint8).reshape(-1))
+    d_in = torch.zeros(n_in, dtype=torch.uint8, device=device)
+
+    def piece(buf, off, a, dtype):
+        return buf[off:off + a.nbytes].view(dtype).view(a.shape)
+
+    g.q = piece(d_in, offs[0], inputs[0], torch.bfloat16)
+    g.new_k = piece(d_in, offs[1], inputs[1], torch.bfloat16)
+    g.new_v = piece(d_in, offs[2], inputs[2], torch.bfloat16)
+    g.cu_new = piece(d_in, offs[3], inputs[3], torch.int32)
+    g.past = piece(d_in, offs[4], inputs[4], torch.int32)
+    g.seq_lens = piece(d_in, offs[5], inputs[5], torch.int32)
+    g.table = piece(d_in, offs[6], inputs[6], torch.int32)
+    g.pages = binding.make_pages(g.table, step.cache.num_blocks)
+
+    outs = [np.empty(tuple(g.out.shape), np.float32), np.empty(tuple(g.lse.shape), np.float32)]
+    o_offs, n_out = layout(outs)
+    d_out = torch.zeros(n_out, dtype=torch.uint8, device=device)
+    g.out = piece(d_out, o_offs[0], outs[0], torch.float32)
+    g.lse = piece(d_out, o_offs[1], outs[1], torch.float32)
+    h_out = torch.zeros(n_out, dtype=torch.uint8).pin_memory()
+    return h_in, d_in, h_out, d_out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,30 +618,17 @@ def main():
     decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     write_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
 
-    # end to end through the C ABI: pinned host inputs in, result back to host
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_q = pin(step.q.view(np.int16))
-    h_k = pin(step.new_k.view(np.int16))
-    h_v = pin(step.new_v.view(np.int16))
-    h_meta = [pin(step.cu_new.astype(np.int32)), pin(step.past_lens.astype(np.int32)),
-              pin(step.seq_lens.astype(np.int32)), pin(step.block_table)]
-    d_meta = [g.cu_new, g.past, g.seq_lens, g.table]
-    h_out = torch.empty(g.out.shape, dtype=torch.float32).pin_memory()
-    h_lse = torch.empty(g.lse.shape, dtype=torch.float32).pin_memory()
-    h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 +
-           sum(t.numel() * 4 for t in h_meta))
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    # end to end through the C ABI: pinned host inputs in, result back to host,
+    # each as one transfer of a packed buffer
+    h_in, d_in, h_out, d_out = packed_step_io(step, g)
+    h2d = h_in.numel()
+    d2h = h_out.numel()
 
     def e2e_step():
-        g.q.view(torch.int16).copy_(h_q, non_blocking=True)
-        g.new_k.view(torch.int16).copy_(h_k, non_blocking=True)
-        g.new_v.view(torch.int16).copy_(h_v, non_blocking=True)
-        for h, d in zip(h_meta, d_meta):
-            d.copy_(h, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         g.write_new()
         g.decode()
-        h_out.copy_(g.out, non_blocking=True)
-        h_lse.copy_(g.lse, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
 
     for _ in range(args.warmup):
