@@ -2,8 +2,9 @@
 layers, then 1 full hd512 k_eq_v layer; 256 decode sequences plus 4 prefill
 chunks of 2048 tokens): every layer runs kv_cache_write, attn_decode_paged and
 attn_prefill_chunked through the C ABI. Outputs are compared with the oracle on
-sampled decode sequences and sampled prefill rows (the whole step is too large
-for an fp64 CPU pass); every output is checked finite."""
+every decode row of the sliding layers, sampled decode rows of the full layer
+and sampled prefill rows (the whole step is too large for an fp64 CPU pass);
+every output is checked finite."""
 import numpy as np
 import pytest
 import torch
@@ -56,8 +57,12 @@ def test_mixed_hybrid_step_all_layers():
                            step.block_table, kp, vp, in_place=True)
         L = step.layer.as_dict()
         lens = step.seq_lens[:nd]
-        seqs = sorted(set(rng.choice(nd, 12, replace=False).tolist() +
-                          [int(np.argmax(lens)), int(np.argmin(lens))]))
+        # every decode row of a sliding layer (at most W keys each); for the
+        # full layer, whose rows reach 65536 keys, the shortest, the longest
+        # and 12 seeded ones
+        sample = sorted(set(rng.choice(nd, 12, replace=False).tolist() +
+                            [int(np.argmax(lens)), int(np.argmin(lens))]))
+        seqs = list(range(nd)) if step.layer.window > 0 else sample
         ref_o, ref_l, _ = orc.decode(L, step.q[:nd], kp, vp, step.block_table[:nd], lens,
                                      seqs=seqs)
         # decode rows are the first nd rows of q/out (one new token each)
