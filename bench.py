@@ -46,12 +46,17 @@ CSRC = os.path.join(ROOT, "paged_sliding_window_gb300", "csrc")
 # ncu summary per measured kernel, and the sources whose hash it was taken at.
 PROFILE_DECODE = ("decode_split_sliding_decode_batch.md", ("decode.cu", "ptx.cuh"))
 PROFILE_PREFILL = ("prefill_chunked_prefill_softcap.md", ("prefill.cu", "ptx.cuh"))
+PROFILE_FULL_DECODE = ("decode_split_full_keqv_decode.md", ("decode.cu", "ptx.cuh"))
+PROFILE_MIXED_PREFILL = ("prefill_mixed_step_full_layer.md", ("prefill.cu", "ptx.cuh"))
 L2_BYTES = 129 * 1024 * 1024
-# kv_cache_write_kernel, decode_plan_kernel, decode_split_kernel
-LAUNCHES_PER_STEP = 3
+# kv_cache_write_kernel, decode_split_kernel
+LAUNCHES_PER_STEP = 2
 
 
 _WORKLOADS = {}
+# host copies of (out, lse) of the last timed call of each workload; the CPU
+# baseline compares the oracle's rows with them
+GPU_OUTPUTS = {}
 
 
 def first_step(name: str) -> wl.Step:
@@ -62,12 +67,14 @@ def first_step(name: str) -> wl.Step:
 
 
 def peaks():
+    """(HBM GB/s, bf16 burst TFLOP/s, "measured" or "fallback", bf16 sustained TFLOP/s)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured",
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])))
+    return 6800.0, 1900.0, "fallback", 1700.0
 
 
 def kv_bytes(step: wl.Step) -> int:
@@ -191,9 +198,25 @@ def oracle_pools(orc, step: wl.Step):
     return kp, vp
 
 
-def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None, threads=0, pools=None):
+def parity_stats(got, ref, atol=2e-3, rtol=1e-2) -> dict:
+    """Elements compared, largest |err| and largest |err| / (atol + rtol |ref|)
+    (1.0 is the bar); -inf matching -inf counts as exact."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    same_inf = np.isneginf(got) & np.isneginf(ref)
+    with np.errstate(invalid="ignore"):
+        err = np.where(same_inf, 0.0, np.abs(got - ref))
+    bar = atol + rtol * np.abs(np.where(same_inf, 0.0, ref))
+    return {"elements": int(got.size), "max_abs_err": float(np.nanmax(err)),
+            "max_err_over_bar": float(np.nanmax(err / bar)),
+            "all_within_bar": bool(np.all(err <= bar))}
+
+
+def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None, threads=0, pools=None, gpu=None,
+                   agreement=None):
     """Times the fp64 oracle on (a subset of) the step; returns
-    (GB/s, threads, description)."""
+    (GB/s, threads, description). With `gpu` = (out, lse) of the GPU call on
+    the same step, the last pass's rows are compared with it into `agreement`."""
     import oracle
     orc = oracle.default()
     kp, vp = oracle_pools(orc, step) if pools is None else pools
@@ -205,24 +228,30 @@ def cpu_oracle_gbs(step: wl.Step, budget_s: float, seqs=None, threads=0, pools=N
     passes, t_total, threads = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
         t0 = time.perf_counter()
-        _, _, used = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table, step.seq_lens,
-                                seqs=idx, threads=threads)
+        ref_o, ref_l, used = orc.decode(L.as_dict(), step.q, kp, vp, step.block_table,
+                                        step.seq_lens, seqs=idx, threads=threads)
         t_total += time.perf_counter() - t0
         passes += 1
     gbs = nbytes * passes / t_total / 1e9
     desc = (f"fp64 C oracle, {len(idx)} of {step.n_seqs} sequences x all heads, "
             f"{passes} passes in {t_total:.1f} s")
+    if gpu is not None:
+        agreement.update(rows=f"the {len(idx)} sequences of this sample",
+                         out=parity_stats(gpu[0][idx], ref_o),
+                         lse=parity_stats(gpu[1][idx], ref_l))
     return gbs, used, desc
 
 
-def cpu_oracle_prefill(step: wl.Step, budget_s: float, every: int = 64):
-    """Times the fp64 oracle on every `every`-th chunk row of a prefill step;
-    returns (TFLOP/s counting visible pairs, threads, description)."""
+def cpu_oracle_prefill(step: wl.Step, budget_s: float, every: int = 64, threads: int = 0,
+                       pools=None, first_seq: int = 0, gpu=None, agreement=None):
+    """Times the fp64 oracle on every `every`-th chunk row of a prefill step
+    (chunks of sequences first_seq.. only); returns (TFLOP/s counting visible
+    pairs, threads, description)."""
     import oracle
     orc = oracle.default()
-    kp, vp = oracle_pools(orc, step)
+    kp, vp = oracle_pools(orc, step) if pools is None else pools
     L = step.layer
-    rows = np.arange(0, int(step.cu_new[-1]), every, dtype=np.int64)
+    rows = np.arange(int(step.cu_new[first_seq]), int(step.cu_new[-1]), every, dtype=np.int64)
     seq_of = np.searchsorted(step.cu_new, rows, side="right") - 1
     pos = step.past_lens[seq_of].astype(np.int64) + rows - step.cu_new[seq_of]
     vis = np.minimum(pos + 1, L.window) if L.window > 0 else pos + 1
@@ -230,25 +259,75 @@ def cpu_oracle_prefill(step: wl.Step, budget_s: float, every: int = 64):
     passes, t_total, used = 0, 0.0, 0
     while passes == 0 or t_total < budget_s:
         t0 = time.perf_counter()
-        _, _, used = orc.prefill(L.as_dict(), step.q, step.cu_new, step.past_lens, kp, vp,
-                                 step.block_table, rows=rows)
+        ref_o, ref_l, used = orc.prefill(L.as_dict(), step.q, step.cu_new, step.past_lens, kp,
+                                         vp, step.block_table, rows=rows, threads=threads)
         t_total += time.perf_counter() - t0
         passes += 1
     rate = flops * passes / t_total / 1e12
-    desc = (f"fp64 C oracle, every {every}th of {int(step.cu_new[-1])} chunk rows x all heads, "
+    n_rows = int(step.cu_new[-1]) - int(step.cu_new[first_seq])
+    desc = (f"fp64 C oracle, every {every}th of {n_rows} chunk rows x all heads, "
             f"{passes} passes in {t_total:.1f} s")
+    if gpu is not None:
+        agreement.update(rows=f"the {len(rows)} chunk rows of this sample",
+                         out=parity_stats(gpu[0][rows], ref_o),
+                         lse=parity_stats(gpu[1][rows], ref_l))
     return rate, used, desc
 
 
 def cpu_oracle_extra(budget_s: float) -> dict:
-    """Oracle rates on the host cores for the other workloads (bounded samples)."""
+    """Oracle rates on the host cores for the other workloads (bounded
+    samples), with all cores and with one."""
+    import oracle
+    orc = oracle.default()
+    out = {}
     step = first_step("full_keqv_decode")
-    gbs, cores, desc = cpu_oracle_gbs(step, budget_s, seqs=np.arange(0, step.n_seqs, 4))
-    out = {"full_keqv_decode": {"value": gbs, "unit": "GB/s", "cores": cores, "sample": desc}}
+    pools = oracle_pools(orc, step)
+    agree = {}
+    gbs, cores, desc = cpu_oracle_gbs(step, budget_s, seqs=np.arange(step.n_seqs), pools=pools,
+                                      gpu=GPU_OUTPUTS.get("full_keqv_decode"), agreement=agree)
+    gbs1, _, desc1 = cpu_oracle_gbs(step, budget_s / 2, seqs=np.arange(0, step.n_seqs, 16),
+                                    threads=1, pools=pools)
+    out["full_keqv_decode"] = {"value": gbs, "unit": "GB/s", "cores": cores, "sample": desc,
+                               "single_core": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                                               "sample": desc1},
+                               "gpu_agreement": agree or None}
+    del pools
     step = first_step("chunked_prefill")
-    tf, cores, desc = cpu_oracle_prefill(step, budget_s)
-    out["prefill"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "sample": desc}
+    pools = oracle_pools(orc, step)
+    agree = {}
+    tf, cores, desc = cpu_oracle_prefill(step, budget_s, every=1, pools=pools,
+                                         gpu=GPU_OUTPUTS.get("chunked_prefill"), agreement=agree)
+    tf1, _, desc1 = cpu_oracle_prefill(step, budget_s / 2, every=512, threads=1, pools=pools)
+    out["prefill"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "sample": desc,
+                      "single_core": {"value": tf1, "unit": "TFLOP/s", "cores": 1,
+                                      "sample": desc1},
+                      "gpu_agreement": agree or None}
+    del pools
+    out["mixed_hybrid_step"] = cpu_oracle_mixed(budget_s)
     return out
+
+
+def cpu_oracle_mixed(budget_s: float) -> dict:
+    """The oracle on a deterministic sample of the mixed 6-layer step: the
+    first sliding layer and the full k_eq_v layer, each with every 4th decode
+    sequence and every 64th prefill chunk row, timed with all cores."""
+    import oracle
+    orc = oracle.default()
+    work = wl.mixed_hybrid(threads=16)
+    nd = work.decode_seqs
+    res = {}
+    for name, li in (("sliding_layer", 0), ("full_layer", 5)):
+        step = work.steps[li]
+        pools = oracle_pools(orc, step)
+        gbs, cores, desc = cpu_oracle_gbs(step, budget_s / 2, seqs=np.arange(0, nd, 4),
+                                          pools=pools)
+        tf, _, pdesc = cpu_oracle_prefill(step, budget_s / 2, every=64, pools=pools,
+                                          first_seq=nd)
+        res[name] = {"decode": {"value": gbs, "unit": "GB/s", "cores": cores, "sample": desc},
+                     "prefill": {"value": tf, "unit": "TFLOP/s", "cores": cores,
+                                 "sample": pdesc}}
+        del pools
+    return res
 
 
 def run_reference(args, rank, world):
@@ -355,6 +434,7 @@ def measure_prefill(steps, warmup, tflops_peak, peak_kind):
     torch.cuda.synchronize()
     assert binding.get_error() == 0
     achieved = flops / (call_ms / 1e3) / 1e12
+    GPU_OUTPUTS["chunked_prefill"] = (g.out.cpu().numpy(), g.lse.cpu().numpy())
     return {"workload": "chunked prefill with softcap", "metric": "prefill attn TFLOP/s",
             "value": achieved, "unit": "TFLOP/s", "ms_per_call": call_ms,
             "kv_cache_write_ms": write_ms, "flops_per_call": flops,
@@ -364,8 +444,11 @@ def measure_prefill(steps, warmup, tflops_peak, peak_kind):
             "roofline": {"bound": "tensor", "kernel": "prefill_kernel<256, false>",
                          "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
                          "frac": achieved / tflops_peak, "peak_kind": peak_kind + " bf16 burst",
-                         "traffic": profiled_traffic(PROFILE_PREFILL)},
-            "gpu_launches_per_call": 1}
+                         "frac_of_sustained": achieved / peaks()[3],
+                         "traffic": profiled_traffic(PROFILE_PREFILL),
+                         "traffic_source": "committed ncu summary (DRAM read + write per launch),"
+                                           " null once the kernel source changed"},
+            "gpu_launches_per_call": 2}
 
 
 def measure_full_decode(steps, warmup, hbm, peak_kind):
@@ -381,14 +464,19 @@ def measure_full_decode(steps, warmup, hbm, peak_kind):
     assert binding.get_error() == 0
     gbs = nbytes / (call_ms / 1e3) / 1e9
     achieved = (nbytes + io_bytes(step)) / (call_ms / 1e3) / 1e9
+    GPU_OUTPUTS["full_keqv_decode"] = (g.out.cpu().numpy(), g.lse.cpu().numpy())
     return {"workload": "full-layer k_eq_v decode", "metric": "decode attn KV-read GB/s",
             "value": gbs, "unit": "GB/s", "ms_per_call": call_ms, "kv_bytes_per_call": nbytes,
             "config": {"n_seqs": 32, "seq_len": "log-uniform [1024, 32768]", "head_dim": 512,
                        "n_q_heads": 32, "n_kv_heads": 4, "k_eq_v": True,
                        "l2": "inputs larger than L2, no flush"},
-            "roofline": {"bound": "hbm", "kernel": "attn_decode_paged (plan + split + merge)",
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<512, true>",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None}}
+                         "frac": achieved / hbm, "peak_kind": peak_kind,
+                         "traffic": profiled_traffic(PROFILE_FULL_DECODE),
+                         "traffic_source": "committed ncu summary (DRAM read + write per launch),"
+                                           " null once the kernel source changed"},
+            "gpu_launches_per_call": 1}
 
 
 def decode_kv_bytes_subset(step: wl.Step, n: int) -> int:
@@ -446,15 +534,32 @@ def measure_mixed(steps, warmup):
     t_write = statistics.mean(sum(r[i][0].elapsed_time(r[i][1]) for i in range(6)) for r in evs)
     t_dec = statistics.mean(sum(r[i][1].elapsed_time(r[i][2]) for i in range(6)) for r in evs)
     t_pre = statistics.mean(sum(r[i][2].elapsed_time(r[i][3]) for i in range(6)) for r in evs)
+    t_pre_full = statistics.mean(r[5][2].elapsed_time(r[5][3]) for r in evs)
+    t_dec_full = statistics.mean(r[5][1].elapsed_time(r[5][2]) for r in evs)
     t_step = statistics.mean(r[0][0].elapsed_time(r[5][3]) for r in evs)
     dec_bytes = sum(decode_kv_bytes_subset(m.step, nd) for m in layers)
     pre_flops = sum(prefill_flops_subset(m.step, nd) for m in layers)
+    full_flops = prefill_flops_subset(layers[5].step, nd)
+    full_bytes = decode_kv_bytes_subset(layers[5].step, nd)
+    hbm, tf, kind, tf_sus = peaks()
+    full_rate = full_flops / (t_pre_full / 1e3) / 1e12
     return {"workload": "mixed hybrid step (6 layers, 256 decode + 4 x 2048 prefill)",
             "ms_per_step": t_step, "kv_cache_write_ms": t_write, "decode_ms": t_dec,
             "prefill_ms": t_pre, "decode_kv_bytes": dec_bytes,
             "decode_GBps": dec_bytes / (t_dec / 1e3) / 1e9, "prefill_flops": pre_flops,
             "prefill_TFLOPs": pre_flops / (t_pre / 1e3) / 1e12,
-            "gpu_launches_per_step": 6 * (1 + 2 + 1)}
+            "prefill_frac_of_burst": pre_flops / (t_pre / 1e3) / 1e12 / tf,
+            "full_layer": {"prefill_ms": t_pre_full, "prefill_flops": full_flops,
+                           "prefill_TFLOPs": full_rate, "decode_ms": t_dec_full,
+                           "decode_GBps": full_bytes / (t_dec_full / 1e3) / 1e9},
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel<512, true> (full layer)",
+                         "achieved": full_rate, "peak": tf, "unit": "TFLOP/s",
+                         "frac": full_rate / tf, "frac_of_sustained": full_rate / tf_sus,
+                         "peak_kind": kind + " bf16 burst",
+                         "traffic": profiled_traffic(PROFILE_MIXED_PREFILL),
+                         "traffic_source": "committed ncu summary of the full layer's prefill "
+                                           "launch, null once the kernel source changed"},
+            "gpu_launches_per_step": 6 * (1 + 1 + 2)}
 
 
 def ncu_case(which):
@@ -464,7 +569,21 @@ def ncu_case(which):
     from paged_sliding_window_gb300 import build
     from paged_sliding_window_gb300.staging import GpuStep
     build.build()
-    if which == "decode":
+    if which == "full_decode":
+        step = first_step("full_keqv_decode")
+        g = GpuStep(step)
+        g.write_new()
+        for _ in range(3):
+            g.decode()
+    elif which == "mixed_full_prefill":
+        _, pre_past = wl.mixed_hybrid_lengths()
+        step = wl.custom_step(wl.FULL_512_KEQV, 5, pre_past, np.full(len(pre_past), 2048),
+                              threads=8)
+        g = GpuStep(step)
+        g.write_new()
+        for _ in range(3):
+            g.prefill()
+    elif which == "decode":
         full = wl.sliding_decode().steps[0]
         ss = np.random.SeedSequence(2)
         rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
@@ -541,7 +660,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the prefill, full-layer decode and mixed-step measurements")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill"], default=None)
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "full_decode",
+                                           "mixed_full_prefill"], default=None)
     args = ap.parse_args()
     if args.ncu_case:
         ncu_case(args.ncu_case)
@@ -617,6 +737,7 @@ def main():
                                 "step, untimed, sampled every 200 ms")
     decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     write_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    GPU_OUTPUTS["sliding_decode"] = (g.out.cpu().numpy(), g.lse.cpu().numpy())
 
     # end to end through the C ABI: pinned host inputs in, result back to host,
     # each as one transfer of a packed buffer
@@ -646,7 +767,7 @@ def main():
     value = whole_job_rate(nbytes, world, ms_per_step / 1e3) / 1e9
     e2e_value = whole_job_rate(nbytes, world, e2e_s) / 1e9
 
-    hbm, _, peak_kind = peaks()
+    hbm, _, peak_kind, _ = peaks()
     achieved = (nbytes + io_bytes(step)) / (decode_ms / 1e3) / 1e9
     traffic = profiled_traffic()
     line = {
@@ -664,7 +785,7 @@ def main():
         "clocks": clock_info,
     }
     if not args.no_extra:
-        hbm_p, tf_p, kind_p = peaks()
+        hbm_p, tf_p, kind_p, _ = peaks()
         line["prefill"] = measure_prefill(args.steps, args.warmup, tf_p, kind_p)
         line["full_keqv_decode"] = measure_full_decode(args.steps, args.warmup, hbm_p, kind_p)
         if not args.no_mixed:
@@ -672,9 +793,11 @@ def main():
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         import oracle
         pools = oracle_pools(oracle.default(), step)
-        gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget, pools=pools)
+        agree = {}
+        gbs, cores, desc = cpu_oracle_gbs(step, args.cpu_budget, pools=pools,
+                                          gpu=GPU_OUTPUTS["sliding_decode"], agreement=agree)
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "gpu_agreement": agree}
         gbs1, _, desc1 = cpu_oracle_gbs(step, args.cpu_budget / 4, seqs=np.arange(0, 64, 8),
                                         threads=1, pools=pools)
         line["cpu_baseline"]["single_core"] = {"value": gbs1, "unit": UNIT, "cores": 1,

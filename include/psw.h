@@ -115,9 +115,18 @@ typedef struct {
  * Workspace bytes that attn_decode_paged and attn_prefill_chunked need for a
  * batch of up to n_seqs sequences (max_seq_len bounds every seq_len and every
  * past_len + chunk length). Pure host arithmetic; needs no GPU. The same
- * workspace may be reused by consecutive calls on one stream.
+ * workspace may be reused by consecutive calls on one stream; when several
+ * calls share it, size it for the largest of them.
+ *
+ * Zeroing rule: the first PSW_WORKSPACE_COUNTER_BYTES bytes of a workspace
+ * hold the merge tickets of attn_decode_paged. They must be zero before the
+ * first call that uses the workspace (zero-fill the buffer once when it is
+ * allocated); every call leaves them zero again, so no call needs a reset.
+ * Only a call that flagged PSW_DEVERR_PIPELINE may leave them non-zero; zero
+ * them again before reusing that workspace.
  * Returns PSW_OK and writes *bytes, or an argument error.
  */
+#define PSW_WORKSPACE_COUNTER_BYTES 2048
 PSW_API int psw_workspace_bytes(const psw_layer_t *layer, int32_t n_seqs, int32_t max_seq_len,
                         size_t *bytes);
 
@@ -150,9 +159,12 @@ PSW_API int kv_cache_write(const psw_layer_t *layer, const void *k, const void *
  *   seq_lens   device int32 [n_seqs]; 0 gives a zero row and lse = -inf
  *   out        device fp32 [n_seqs][n_q_heads][head_dim]
  *   lse        device fp32 [n_seqs][n_q_heads] or NULL
- *   ws         device workspace of ws_bytes >= psw_workspace_bytes(layer, n_seqs, .)
- * Split-KV flash decoding: partial results over page ranges go to the
- * workspace and a log-sum-exp merge combines them.
+ *   ws         device workspace of ws_bytes >= psw_workspace_bytes(layer, n_seqs, .),
+ *              zero-filled once before its first use (see the zeroing rule above)
+ * Split-KV flash decoding in one kernel launch: every CTA derives its share of
+ * the work from seq_lens, partial results over page ranges go to the
+ * workspace, and the CTA that finishes a sequence's last range combines them
+ * with the log-sum-exp rule.
  */
 PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const void *k_pool,
                       const void *v_pool, const psw_pages_t *pages,
@@ -173,7 +185,8 @@ PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const voi
  *              chunks are flagged (PSW_DEVERR_LENGTH) and their excess rows skipped
  *   out        device fp32 [n_q_total][n_q_heads][head_dim]; lse fp32 [n_q_total][n_q_heads] or NULL
  *   ws         device workspace of ws_bytes >= psw_workspace_bytes(layer, n_seqs, L)
- *              for any L >= max_q_len; it holds the work list of the call
+ *              for any L >= max_q_len; it holds the work list of the call after
+ *              the counter block, which this call neither reads nor writes
  * Tensor-core kernel (tcgen05 MMAs with S, P and O in tensor memory, K/V tiles
  * fed by TMA through the block table); key tiles that the band rule hides from
  * every row of a query tile are never loaded. A small plan kernel first orders
@@ -196,17 +209,25 @@ PSW_API int attn_prefill_chunked(const psw_layer_t *layer, const void *q, const 
  *
  * Arguments, results and errors are those of attn_decode_paged, without the
  * workspace: the scratch comes from a static device buffer of
- * PSW_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the
- * library holds until the process exits. A batch whose workspace
- * (psw_workspace_bytes) exceeds that size returns PSW_ESCRATCH before anything
- * runs: with head_dim 256 that is more than about 1500 units, with head_dim
- * 512 more than about 500, where units = n_seqs * n_kv_heads *
+ * PSW_NOALLOC_SCRATCH_BYTES inside the library. Pointer and alignment errors
+ * are reported first, as by attn_decode_paged; then a batch whose workspace
+ * (psw_workspace_bytes) exceeds the buffer returns PSW_ESCRATCH before
+ * anything runs: with head_dim 256 that is more than about 1500 units, with
+ * head_dim 512 more than about 500, where units = n_seqs * n_kv_heads *
  * ceil((n_q_heads / n_kv_heads) / 8).
  *
- * The first call on a device looks up the buffer's device address (with that
- * device current) and keeps it; make that first call before any stream
- * capture. Nothing is allocated or freed, ever. All calls share the buffer and
- * it keeps the last call's contents; nothing in it needs to start at zero.
+ * Set-up: the first call on a device looks up the buffer's device address
+ * (with that device current) and keeps it. Under CUDA's lazy module loading
+ * (the default) that lookup is also when the driver loads the library's
+ * module holding the buffer and reserves its memory on the device, so that
+ * step can fail (PSW_EDEVICE) if the device is out of memory. Make the first
+ * call at start-up, before any stream capture: a call with n_seqs = 0 and
+ * valid pointers does the set-up and launches nothing. From then on the
+ * buffer stays reserved on that device until the process exits, and nothing
+ * is allocated or freed by this entry point.
+ *
+ * All calls share the buffer and it keeps the last call's contents; its
+ * counters start at zero (static storage) and every call leaves them zero.
  * Calls whose kernels could overlap on the GPU (several streams or host
  * threads on one device) race on the buffer: serialise them.
  */

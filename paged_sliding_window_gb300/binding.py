@@ -140,9 +140,13 @@ def workspace_bytes(layer, n_seqs: int, max_seq_len: int) -> int:
     return int(out.value)
 
 
+WORKSPACE_COUNTER_BYTES = 2048  # PSW_WORKSPACE_COUNTER_BYTES
+
+
 def alloc_workspace(layer, n_seqs: int, max_seq_len: int, device="cuda") -> torch.Tensor:
-    """A caller-owned workspace of the size the library asks for."""
-    return torch.empty(max(workspace_bytes(layer, n_seqs, max_seq_len), 256), dtype=torch.uint8,
+    """A caller-owned workspace of the size the library asks for, zero-filled
+    once (its counter block must start at zero; calls keep it zero)."""
+    return torch.zeros(max(workspace_bytes(layer, n_seqs, max_seq_len), 256), dtype=torch.uint8,
                        device=device)
 
 

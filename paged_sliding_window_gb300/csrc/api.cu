@@ -117,7 +117,45 @@ int device_ready(DeviceState** st) {
   return PSW_OK;
 }
 
+struct SmemLimitSet {
+  const void* kernel;
+  int device;
+};
+std::mutex g_attr_mutex;
+SmemLimitSet g_attr_done[256];
+int g_attr_count = 0;
+
 }  // namespace
+
+int set_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PSW_EDEVICE;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  for (int i = 0; i < g_attr_count; ++i)
+    if (g_attr_done[i].kernel == kernel && g_attr_done[i].device == dev) return PSW_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return PSW_ELAUNCH;
+  // a full table only means the attribute is set again on later calls
+  if (g_attr_count < static_cast<int>(sizeof(g_attr_done) / sizeof(g_attr_done[0])))
+    g_attr_done[g_attr_count++] = SmemLimitSet{kernel, dev};
+  return PSW_OK;
+}
+
+int check_decode_args(const psw_layer_t* layer, const void* q, const void* k_pool,
+                      const void* v_pool, const psw_pages_t* pages, const int32_t* seq_lens,
+                      int32_t n_seqs, const float* out, LayerArgs* L) {
+  int rc = check_layer(layer, L);
+  if (rc != PSW_OK) return rc;
+  if (q == nullptr || k_pool == nullptr || seq_lens == nullptr || out == nullptr)
+    return PSW_ENULL;
+  if ((rc = check_v(*L, v_pool)) != PSW_OK) return rc;
+  if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PSW_EALIGN;
+  return PSW_OK;
+}
 
 cudaError_t device_info(DeviceInfo* info) {
   DeviceState* st = current_device();
@@ -235,15 +273,8 @@ int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_poo
                       int32_t n_seqs, float* out, float* lse, void* ws, size_t ws_bytes,
                       psw_stream_t stream) {
   LayerArgs L;
-  int rc = check_layer(layer, &L);
+  int rc = check_decode_args(layer, q, k_pool, v_pool, pages, seq_lens, n_seqs, out, &L);
   if (rc != PSW_OK) return rc;
-  if (q == nullptr || k_pool == nullptr || seq_lens == nullptr || out == nullptr)
-    return PSW_ENULL;
-  if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
-  if ((rc = check_pages(pages)) != PSW_OK) return rc;
-  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
-    return PSW_EALIGN;
   if (n_seqs == 0) return PSW_OK;
   if (ws == nullptr) return PSW_EWORKSPACE;
   if (ws_bytes < decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total) return PSW_EWORKSPACE;

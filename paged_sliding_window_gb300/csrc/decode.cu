@@ -51,18 +51,12 @@ constexpr int kChunkBytes = kBlockSize * 128;  // one TMA box: 16 rows x 128 B
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct SeqPlan {
-  int32_t tile_off;  // first tile of this sequence in the global tile list
-  int32_t len;       // seq_len after validation
-  int32_t lo;        // first visible position
-  int32_t ntu;       // tiles per unit
-};
-
 // Two CTAs share each SM: every tile is 32 KB of K/V (2 pages of K and V, or
 // 4 pages of K alone with k_eq_v at head_dim 256, ...), 3 tiles in flight per
 // CTA, so each SM keeps two independent TMA pipelines and 8 consumer warps.
 constexpr int kCtasPerSm = 2;
 constexpr int kStageTarget = 32768;
+constexpr int kInfoInts = 16;  // shared ints: warp sums, slice start, flags
 
 template <int HD, bool KEQV>
 struct Cfg {
@@ -81,7 +75,7 @@ struct Cfg {
   static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kSRow;
   static constexpr int kTmaPerTile = kTilePages * kChunks * (KEQV ? 1 : 2);
   static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + 64;
+      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + kInfoInts * 4;
   static_assert(kTilePages >= 1, "tile of at least one page");
   static_assert(kTmaPerTile <= 32, "one TMA box per producer lane");
   static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory per SM");
@@ -93,94 +87,50 @@ __device__ __forceinline__ int sbuf_key(int qh, int key) {
   return key ^ (((qh ^ (qh >> 2)) & 3) << 3);
 }
 
-// ---------------------------------------------------------------- plan
-// One CTA: validates seq_lens, computes per-sequence tile counts and their
-// exclusive prefix. plan[n_seqs].tile_off holds the total.
-// It also zeroes the merge tickets of every unit and writes the output of
-// empty sequences (zeros, lse = -inf), which have no tiles.
-__global__ void __launch_bounds__(1024)
-decode_plan_kernel(const int32_t* __restrict__ seq_lens, int n_seqs, int window,
-                   int max_blocks, int units_per_seq, int tile_pages,
-                   SeqPlan* __restrict__ plan, int32_t* __restrict__ tickets, int row_floats,
-                   int n_q, float* __restrict__ out, float* __restrict__ lse, int32_t* err) {
-  __shared__ int32_t warp_tot[32];
-  __shared__ int32_t carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < n_seqs * units_per_seq; i += blockDim.x) tickets[i] = 0;
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  const int cap = max_blocks * kBlockSize;
-  for (int base = 0; base < n_seqs; base += blockDim.x) {
-    const int s = base + tid;
-    int len = 0, lo = 0, ntu = 0;
-    if (s < n_seqs) {
-      len = seq_lens[s];
-      if (len < 0) { flag_error(err, PSW_DEVERR_LENGTH); len = 0; }
-      if (len > cap) { flag_error(err, PSW_DEVERR_CAPACITY); len = cap; }
-      lo = (window > 0 && len > window) ? len - window : 0;
-      if (len > 0) {
-        const int npages = (len - 1) / kBlockSize - lo / kBlockSize + 1;
-        ntu = (npages + tile_pages - 1) / tile_pages;
-      }
-    }
-    const int tiles = ntu * units_per_seq;
-    int incl = tiles;
-    #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int nw = blockDim.x >> 5;
-      int w = lane < nw ? warp_tot[lane] : 0;
-      #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, w, o);
-        if (lane >= o) w += v;
-      }
-      warp_tot[lane] = w;  // inclusive prefix over warps
-    }
-    __syncthreads();
-    const int excl = incl - tiles + (warp > 0 ? warp_tot[warp - 1] : 0);
-    if (s < n_seqs) plan[s] = SeqPlan{carry + excl, len, lo, ntu};
-    if (s < n_seqs && ntu == 0) {  // no visible key: zero output, lse = -inf
-      float4* row = reinterpret_cast<float4*>(out + static_cast<int64_t>(s) * row_floats);
-      for (int i = 0; i < row_floats / 4; ++i) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (lse != nullptr)
-        for (int i = 0; i < n_q; ++i) lse[static_cast<int64_t>(s) * n_q + i] = -INFINITY;
-    }
-    __syncthreads();
-    if (tid == 0) carry += warp_tot[(blockDim.x >> 5) - 1];
-    __syncthreads();
+// ---------------------------------------------------------------- sequences
+// What one sequence contributes to the tile list, from its seq_len alone: the
+// length after validation (negative -> 0, longer than the block-table row ->
+// the row's capacity), the first visible position (only the last min(len, W)
+// keys of a sliding layer) and the tiles of each of its units.
+struct SeqInfo {
+  int len, lo, ntu;
+};
+__device__ __forceinline__ SeqInfo seq_info(const int32_t* __restrict__ seq_lens, int s,
+                                            int window, int cap, int tile_pages) {
+  int len = seq_lens[s];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int lo = (window > 0 && len > window) ? len - window : 0;
+  int ntu = 0;
+  if (len > 0) {
+    const int npages = (len - 1) / kBlockSize - lo / kBlockSize + 1;
+    ntu = (npages + tile_pages - 1) / tile_pages;
   }
-  if (tid == 0) plan[n_seqs] = SeqPlan{carry, 0, 0, 0};
+  return SeqInfo{len, lo, ntu};
 }
 
 // ---------------------------------------------------------------- walker
-// Iterates the global tile list in order: sequence, unit, tile.
+// Iterates the global tile list in order: sequence, unit, tile. Sequence
+// data comes straight from seq_lens; tile_off (the first tile of the current
+// sequence) is carried along.
 struct Walker {
-  const SeqPlan* plan;
-  int n_seqs, ups;
+  const int32_t* seq_lens;
+  int n_seqs, ups, window, cap, tile_pages;
   int s, unit, tile;
   int ntu, len, lo, tile_off;
 
   __device__ void load_seq() {
-    const SeqPlan p = plan[s];
-    tile_off = p.tile_off; len = p.len; lo = p.lo; ntu = p.ntu;
+    const SeqInfo i = seq_info(seq_lens, s, window, cap, tile_pages);
+    len = i.len; lo = i.lo; ntu = i.ntu;
   }
-  __device__ void init(const SeqPlan* pl, int ns, int u, int t) {
-    plan = pl; n_seqs = ns; ups = u;
-    int a = 0, b = ns;  // plan[a].tile_off <= t < plan[b].tile_off
-    while (b - a > 1) {
-      const int mid = (a + b) >> 1;
-      if (plan[mid].tile_off <= t) a = mid; else b = mid;
-    }
-    s = a;
+  // s0 holds tile t and its first tile is off0
+  __device__ void init(const int32_t* sl, int ns, int u, int win, int cp, int tp, int s0,
+                       int off0, int t) {
+    seq_lens = sl; n_seqs = ns; ups = u; window = win; cap = cp; tile_pages = tp;
+    s = s0;
+    tile_off = off0;
     load_seq();
     const int rem = t - tile_off;
-    unit = rem / ntu;
+    unit = ntu > 0 ? rem / ntu : 0;
     tile = rem - unit * ntu;
   }
   __device__ void advance() {
@@ -188,11 +138,14 @@ struct Walker {
     tile = 0;
     if (++unit < ups) return;
     unit = 0;
-    do { ++s; } while (s < n_seqs && plan[s + 1].tile_off == plan[s].tile_off);
-    if (s < n_seqs) load_seq();
+    tile_off += ntu * ups;
+    for (++s; s < n_seqs; ++s) {  // sequences without visible keys have no tiles
+      load_seq();
+      if (ntu > 0) break;
+    }
   }
   __device__ int first_page() const { return lo / kBlockSize; }
-  __device__ int last_page() const { return (len - 1) / kBlockSize; }
+  __device__ int last_page() const { return len > 0 ? (len - 1) / kBlockSize : -1; }
   __device__ int unit_first_tile() const { return tile_off + unit * ntu; }
   __device__ int global_unit() const { return s * ups + unit; }
 };
@@ -233,11 +186,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map,
                     const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
-                    int max_blocks, int64_t num_blocks, const SeqPlan* __restrict__ plan,
-                    int n_seqs, int n_q, int n_kv, int group, int qchunks, float scale,
-                    float softcap, float* __restrict__ out, float* __restrict__ lse,
-                    float* __restrict__ ws_o, float2* __restrict__ ws_ml,
-                    int32_t* __restrict__ tickets, int32_t* err) {
+                    int max_blocks, int64_t num_blocks, const int32_t* __restrict__ seq_lens,
+                    int n_seqs, int n_q, int n_kv, int group, int qchunks, int window,
+                    float scale, float softcap, float* __restrict__ out,
+                    float* __restrict__ lse, float* __restrict__ ws_o,
+                    float2* __restrict__ ws_ml, int32_t* __restrict__ tickets, int32_t* err) {
   using C = Cfg<HD, KEQV>;
   constexpr int TP = C::kTilePages;
   extern __shared__ uint8_t smem_raw[];
@@ -250,6 +203,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + C::kStages);
   volatile int* cons_abort = abort_flag + 1;  // written only by consumer warps
   volatile int* merge_flag = abort_flag + 2;  // this CTA merges the current unit
+  int* info = const_cast<int*>(abort_flag) + 4;  // warp sums [0, 5), slice start [5, 7)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -268,18 +222,70 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   }
   __syncthreads();
 
+  // ---- this CTA's slice of the global tile list. Every CTA forms the same
+  // integer sums over seq_lens: thread i sums the tiles of a contiguous run of
+  // sequences, a block scan gives the total and each run's first tile, and the
+  // thread whose run holds the slice's first tile finds that sequence.
   const int ups = n_kv * qchunks;
-  const int total = plan[n_seqs].tile_off;
+  const int cap = max_blocks * kBlockSize;
+  const int tid = threadIdx.x;
+  const int run = (n_seqs + kThreads - 1) / kThreads;
+  const int s_lo = min(n_seqs, tid * run), s_hi = min(n_seqs, s_lo + run);
+  int mine = 0;
+  for (int s = s_lo; s < s_hi; ++s) mine += seq_info(seq_lens, s, window, cap, TP).ntu * ups;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) info[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int i = 0; i < kConsumerWarps + 1; ++i) {
+    if (i < warp) before += info[i];
+    total += info[i];
+  }
   const int per = (total + gridDim.x - 1) / gridDim.x;
   const int t_begin = blockIdx.x * per;
   const int t_end = min(total, t_begin + per);
+  {
+    int off = before + incl - mine;
+    if (t_begin < t_end && off <= t_begin && t_begin < off + mine) {
+      for (int s = s_lo; s < s_hi; ++s) {
+        const int tl = seq_info(seq_lens, s, window, cap, TP).ntu * ups;
+        if (t_begin < off + tl) {
+          info[5] = s;
+          info[6] = off;
+          break;
+        }
+        off += tl;
+      }
+    }
+  }
+  // Sequences without a visible key have no tiles: CTA s mod grid writes their
+  // zero rows and lse = -inf, and flags invalid lengths of its sequences.
+  for (int s = blockIdx.x; s < n_seqs; s += gridDim.x) {
+    const int raw = seq_lens[s];
+    if (tid == 0 && raw < 0) flag_error(err, PSW_DEVERR_LENGTH);
+    if (tid == 0 && raw > cap) flag_error(err, PSW_DEVERR_CAPACITY);
+    if (raw <= 0) {
+      float4* row = reinterpret_cast<float4*>(out + static_cast<int64_t>(s) * n_q * HD);
+      for (int i = tid; i < n_q * HD / 4; i += kThreads) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lse != nullptr)
+        for (int i = tid; i < n_q; i += kThreads) lse[static_cast<int64_t>(s) * n_q + i] = -INFINITY;
+    }
+  }
+  __syncthreads();
   if (t_begin >= t_end) return;
+  const int start_seq = info[5], start_off = info[6];
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
     Walker w;
-    w.init(plan, n_seqs, ups, t_begin);
+    w.init(seq_lens, n_seqs, ups, window, cap, TP, start_seq, start_off, t_begin);
     // lane -> (K/V, page in tile, chunk) of its TMA box
     const int which = lane / (TP * C::kChunks);
     const int lp = (lane % (TP * C::kChunks)) / C::kChunks;
@@ -293,10 +299,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       const int npages = min(TP, w.last_page() - page0 + 1);
       int blk = -1;
       if (lane < npages) {
-        blk = block_table[static_cast<int64_t>(w.s) * max_blocks + page0 + lane];
-        if (blk < 0 || blk >= num_blocks) {
-          flag_error(err, PSW_DEVERR_BLOCK_ID);
-          blk = -1;  // out-of-range box: TMA fills zeros
+        // the table row is read only inside [0, max_blocks), whatever the walk
+        // says (it stays there by construction: last_page < max_blocks)
+        const int page = page0 + lane;
+        if (page < 0 || page >= max_blocks) {
+          flag_error(err, PSW_DEVERR_CAPACITY);
+        } else {
+          blk = block_table[static_cast<int64_t>(w.s) * max_blocks + page];
+          if (blk < 0 || blk >= num_blocks) {
+            flag_error(err, PSW_DEVERR_BLOCK_ID);
+            blk = -1;  // out-of-range box: TMA fills zeros
+          }
         }
       }
       const int my_blk = __shfl_sync(0xffffffffu, blk, lp);
@@ -365,7 +378,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   const uint32_t stages_u32 = smem_u32(stages);
 
   Walker w;
-  w.init(plan, n_seqs, ups, t_begin);
+  w.init(seq_lens, n_seqs, ups, window, cap, TP, start_seq, start_off, t_begin);
   int consumed = 0;
   for (int t = t_begin; t < t_end; ++t, ++consumed) {
     const int stage = consumed % C::kStages;
@@ -591,11 +604,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       if (!complete) {
         // The CTA that finishes a unit's last segment merges all segments:
         // each CTA publishes its partial, then takes a ticket; nobody waits.
+        // The ticket of a cut unit lives at its first CTA c0 (a CTA starts at
+        // most one cut unit: its last), and the merging CTA, the last to touch
+        // it in this call, sets it back to zero for the next call.
         const int u = w.global_unit();
         const int c0 = uf / per, c1 = (uf + w.ntu - 1) / per;
         __threadfence();
         named_bar_sync(1, kConsumerWarps * 32);
-        if (threadIdx.x == 0) *merge_flag = (atomicAdd(&tickets[u], 1) == c1 - c0);
+        if (threadIdx.x == 0) {
+          const bool last = atomicAdd(&tickets[c0], 1) == c1 - c0;
+          if (last) atomicExch(&tickets[c0], 0);
+          *merge_flag = last;
+        }
         named_bar_sync(1, kConsumerWarps * 32);
         if (*merge_flag) {
           __threadfence();
@@ -619,29 +639,16 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   const DecodeWorkspace lay = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas);
   if (ws_bytes < lay.total) return PSW_EWORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  SeqPlan* plan = reinterpret_cast<SeqPlan*>(base);
   float* ws_o = reinterpret_cast<float*>(base + lay.o_offset);
   float2* ws_ml = reinterpret_cast<float2*>(base + lay.ml_offset);
   int32_t* tickets = reinterpret_cast<int32_t*>(base + lay.ticket_offset);
-
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(decode_split_kernel<HD, KEQV>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return PSW_ELAUNCH;
-    attr_set[dev] = true;
-  }
-  const int ups = L.n_kv * L.qchunks();
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, n_seqs, L.window, max_blocks, ups,
-                                             C::kTilePages, plan, tickets, L.n_q * HD, L.n_q,
-                                             out, lse, err);
+  if (set_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<HD, KEQV>),
+                     C::kSmemBytes) != PSW_OK)
+    return PSW_ELAUNCH;
   decode_split_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
       k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
-      plan, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.scale, L.softcap, out, lse, ws_o,
-      ws_ml, tickets, err);
+      seq_lens, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.window, L.scale, L.softcap,
+      out, lse, ws_o, ws_ml, tickets, err);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 
@@ -652,14 +659,14 @@ DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_
   auto align = [](size_t x) { return (x + kDecodePlanAlign - 1) / kDecodePlanAlign * kDecodePlanAlign; };
   const size_t slots = static_cast<size_t>(max_ctas) +
                        static_cast<size_t>(n_seqs) * L.n_kv * L.qchunks();
-  w.plan_bytes = align((static_cast<size_t>(n_seqs) + 1) * sizeof(dec::SeqPlan));
+  // merge tickets, one per CTA, in the zero-kept counter block at the start
+  w.ticket_offset = 0;
+  w.ticket_bytes = kWsCounterBytes;
   w.o_bytes = align(slots * kQHeadsPerUnit * L.hd * sizeof(float));
   w.ml_bytes = align(slots * kQHeadsPerUnit * sizeof(float2));
-  w.ticket_bytes = align(static_cast<size_t>(n_seqs) * L.n_kv * L.qchunks() * sizeof(int32_t));
-  w.o_offset = w.plan_bytes;
+  w.o_offset = kWsCounterBytes;
   w.ml_offset = w.o_offset + w.o_bytes;
-  w.ticket_offset = w.ml_offset + w.ml_bytes;
-  w.total = w.ticket_offset + w.ticket_bytes;
+  w.total = w.ml_offset + w.ml_bytes;
   return w;
 }
 

@@ -1128,19 +1128,15 @@ int launch(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_ma
            int64_t num_blocks, float* out, float* lse, void* ws, int num_sms, int32_t* err,
            cudaStream_t stream) {
   using C = Cfg<HD, KEQV>;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(prefill_kernel<HD, KEQV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return PSW_ELAUNCH;
-    attr_set[dev] = true;
-  }
+  if (set_smem_limit(reinterpret_cast<const void*>(prefill_kernel<HD, KEQV>), C::kSmemBytes) !=
+      PSW_OK)
+    return PSW_ELAUNCH;
   const int T = kRows / L.group();
   const int max_rb = (max_q_len + T - 1) / T;
-  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws);
-  int2* units = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(ws) + sizeof(PlanHeader));
+  // the work list sits after the counter block, which this call leaves alone
+  uint8_t* wl = static_cast<uint8_t*>(ws) + kWsCounterBytes;
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(wl);
+  int2* units = reinterpret_cast<int2*>(wl + sizeof(PlanHeader));
   prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu_q, past_lens, n_seqs, n_q_total,
                                                       max_q_len, max_blocks, L.window, T, C::kBN,
                                                       max_rb, hdr, units, err);
@@ -1159,7 +1155,8 @@ int launch(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_ma
 size_t prefill_workspace_bytes(const LayerArgs& L, int n_seqs, int max_q_len) {
   const int T = pf::kRows / L.group();
   const size_t max_rb = (static_cast<size_t>(max_q_len > 0 ? max_q_len : 0) + T - 1) / T;
-  const size_t bytes = sizeof(pf::PlanHeader) + static_cast<size_t>(n_seqs) * max_rb * sizeof(int2);
+  const size_t bytes = kWsCounterBytes + sizeof(pf::PlanHeader) +
+                       static_cast<size_t>(n_seqs) * max_rb * sizeof(int2);
   return (bytes + 255) / 256 * 256;
 }
 

@@ -15,6 +15,11 @@ constexpr int kBlockSize = 16;          // tokens per page
 constexpr int kMaxDecodeCtas = 512;     // upper bound on the persistent decode grid
 constexpr int kQHeadsPerUnit = 8;       // query heads handled together per KV head
 constexpr int kDecodePlanAlign = 256;
+// The first kWsCounterBytes of every workspace hold counters that each call
+// leaves at zero (the decode merge tickets, one int32 per CTA); the caller
+// zero-fills a workspace once before its first use (PSW_WORKSPACE_COUNTER_BYTES).
+constexpr size_t kWsCounterBytes = PSW_WORKSPACE_COUNTER_BYTES;
+static_assert(kMaxDecodeCtas * 4 <= PSW_WORKSPACE_COUNTER_BYTES, "one ticket per decode CTA");
 
 struct LayerArgs {
   int n_q, n_kv, hd, window;
@@ -30,15 +35,27 @@ struct DeviceInfo {
   int cc_major, cc_minor;
 };
 
+// Host checks of attn_decode_paged's arguments other than the workspace, in
+// the order that call reports them (layer, pointers, V pool, pages, n_seqs,
+// alignment). Fills *L on success. Returns a PSW_* code.
+int check_decode_args(const psw_layer_t* layer, const void* q, const void* k_pool,
+                      const void* v_pool, const psw_pages_t* pages, const int32_t* seq_lens,
+                      int32_t n_seqs, const float* out, LayerArgs* L);
+
 // Current device's properties (cached per device).
 cudaError_t device_info(DeviceInfo* info);
 
 // Per-device error word used by every kernel (device pointer).
 int32_t* device_error_word();
 
-// Decode workspace layout (bytes): plan | partial O | partial (m, l) | merge tickets.
+// Sets a kernel's dynamic shared-memory limit on the current device, once per
+// (kernel, device); safe to call from several host threads. Returns a PSW_* code.
+int set_smem_limit(const void* kernel, int bytes);
+
+// Decode workspace layout (bytes): merge tickets (counter block) | partial O |
+// partial (m, l).
 struct DecodeWorkspace {
-  size_t plan_bytes, o_bytes, ml_bytes, ticket_bytes, total;
+  size_t o_bytes, ml_bytes, ticket_bytes, total;
   size_t o_offset, ml_offset, ticket_offset;
 };
 DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_ctas);

@@ -308,6 +308,21 @@ def chunked_prefill(seed: int = 4, threads: int = 8, n_seqs: int = 8,
     return Workload("chunked prefill with softcap", seed, "prefill", [step])
 
 
+def _mixed_lengths(rng, n_decode, n_prefill, sigma):
+    dec_lens = lognormal_int(rng, 2048, sigma, 65536, n_decode)
+    pre_past = uniform_int(rng, 0, 16384, n_prefill)
+    return dec_lens, pre_past
+
+
+def mixed_hybrid_lengths(seed: int = 5, n_decode: int = 256, n_prefill: int = 4,
+                         sigma: float = 1.0):
+    """(decode sequence lengths, prefill past lengths) of mixed_hybrid, without
+    drawing any values."""
+    ss = np.random.SeedSequence(seed)
+    rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
+    return _mixed_lengths(rng, n_decode, n_prefill, sigma)
+
+
 def mixed_hybrid(seed: int = 5, threads: int = 8, n_decode: int = 256, n_prefill: int = 4,
                  chunk: int = 2048, sigma: float = 1.0) -> Workload:
     """6-layer hybrid stack in the 5:1 pattern (5 sliding hd256 W=1024 16q/8kv,
@@ -317,8 +332,7 @@ def mixed_hybrid(seed: int = 5, threads: int = 8, n_decode: int = 256, n_prefill
     share one block table; each layer has its own pools and values."""
     ss = np.random.SeedSequence(seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
-    dec_lens = lognormal_int(rng, 2048, sigma, 65536, n_decode)
-    pre_past = uniform_int(rng, 0, 16384, n_prefill)
+    dec_lens, pre_past = _mixed_lengths(rng, n_decode, n_prefill, sigma)
     past = np.concatenate([dec_lens - 1, pre_past])
     new = np.concatenate([np.ones(n_decode, np.int64), np.full(n_prefill, chunk, np.int64)])
     table, nb = deal_block_table(rng, pages_for(past + new))

@@ -17,3 +17,18 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Per comparison of the GPU parity tests: elements compared, the largest
+    absolute error and the largest |err| / (2e-3 + 1e-2 |ref|) (the bar is 1)."""
+    mod = sys.modules.get("gpu_harness")
+    log = getattr(mod, "PARITY_LOG", None) if mod else None
+    if not log:
+        return
+    tr = terminalreporter
+    tr.section("parity against the fp64 oracle")
+    tr.write_line(f"{'test / output':<92} {'elements':>11} {'max|err|':>10} {'err/bar':>8}")
+    for test, what, n, e, r in log:
+        name = f"{test.split('::', 1)[-1]} / {what}"
+        tr.write_line(f"{name[:92]:<92} {n:>11} {e:>10.3e} {r:>8.3f}")

@@ -4,6 +4,8 @@ same seeded inputs and each writes the history into its own canary-filled
 pools with its own cache write."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch  # noqa: F401
 
@@ -43,6 +45,11 @@ class OracleStep:
         return out, lse
 
 
+# (test, what, elements, max |err|, max |err| / (atol + rtol |ref|)) of every
+# comparison in this session; conftest prints them at the end of the run
+PARITY_LOG: list = []
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rtol=RTOL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -50,6 +57,13 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rtol=RT
     both_neg_inf = np.isneginf(got) & np.isneginf(ref)
     err = np.abs(got - ref)
     bad = ~((err <= atol + rtol * np.abs(ref)) | both_neg_inf)
+    finite = ~both_neg_inf
+    with np.errstate(invalid="ignore"):
+        e = np.where(finite, err, 0.0)
+        ratio = np.where(finite, err / (atol + rtol * np.abs(np.where(finite, ref, 0.0))), 0.0)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    PARITY_LOG.append((test, what, int(got.size), float(np.nanmax(e)) if e.size else 0.0,
+                       float(np.nanmax(ratio)) if ratio.size else 0.0))
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(

@@ -57,24 +57,30 @@ FULL = Layer(n_q_heads=32, n_kv_heads=4, head_dim=512, window=0, k_eq_v=True)
 
 
 def test_workspace_bytes_arithmetic(lib):
-    # plan + (max CTAs + units) slots of 8 query heads x (head_dim floats + (m, l)) + tickets
-    # and, for prefill, a 64-byte header plus one 8-byte entry per block of
-    # 128 / G chunk tokens of every sequence; the larger of the two
+    # a 2048-byte counter block (one merge ticket per decode CTA), then for
+    # decode (max CTAs + units) slots of 8 query heads x (head_dim floats +
+    # (m, l)), and for prefill a 64-byte header plus one 8-byte entry per
+    # block of 128 / G chunk tokens of every sequence; the larger of the two
     def expect(layer, n_seqs, max_len):
         G = layer.n_q_heads // layer.n_kv_heads
         units = n_seqs * layer.n_kv_heads * ((G + 7) // 8)
         slots = 512 + units
         align = lambda x: (x + 255) // 256 * 256
-        decode = (align((n_seqs + 1) * 16) + align(slots * 8 * layer.head_dim * 4) +
-                  align(slots * 8 * 8) + align(units * 4))
+        decode = 2048 + align(slots * 8 * layer.head_dim * 4) + align(slots * 8 * 8)
         T = 128 // G
-        prefill = align(64 + n_seqs * ((max_len + T - 1) // T) * 8)
+        prefill = align(2048 + 64 + n_seqs * ((max_len + T - 1) // T) * 8)
         return max(decode, prefill)
     for layer, n, max_len in ((SLIDING, 64, 4096), (FULL, 32, 4096), (SLIDING, 0, 4096),
                               (FULL, 1000, 4096), (FULL, 4, 1 << 24), (SLIDING, 2, 0)):
         assert binding.workspace_bytes(layer, n, max_len) == expect(layer, n, max_len)
     # the prefill term dominates for few, very long sequences
     assert expect(FULL, 4, 1 << 24) > expect(FULL, 4, 4096)
+
+
+def test_counter_block_size_matches_header():
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+PSW_WORKSPACE_COUNTER_BYTES\s+(\d+)", text)
+    assert m and int(m.group(1)) == binding.WORKSPACE_COUNTER_BYTES
 
 
 FAKE = 0x10000  # aligned fake device address; validation never dereferences
@@ -190,3 +196,32 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     """No silent CPU path: a valid call on a host without a GPU is refused."""
     assert _decode(lib, _layer()) == -13
     assert _write(lib, _layer()) == -13
+
+
+def _noalloc(lib, layer, q=FAKE, k=FAKE, v=FAKE, pages=None, seq=FAKE, n=4, out=FAKE):
+    pages = pages or _pages()
+    return lib.attn_decode_paged_noalloc(ctypes.byref(layer), q, k, v, ctypes.byref(pages), seq,
+                                         n, out, None, None)
+
+
+def test_noalloc_reports_argument_errors_before_the_scratch_limit(lib):
+    """The no-allocation decode checks pointers and alignment like
+    attn_decode_paged before it compares the batch with its static buffer."""
+    layer = _layer()
+    too_many = 4096  # far beyond the static buffer at head_dim 256
+    assert binding.workspace_bytes(SLIDING, too_many, 1) > 16 * 1024 * 1024
+    assert _noalloc(lib, layer, q=None, n=too_many) == -1
+    assert _noalloc(lib, layer, out=None, n=too_many) == -1
+    assert _noalloc(lib, layer, q=FAKE + 8, n=too_many) == -12
+    assert _noalloc(lib, layer, v=None, n=too_many) == -7
+    assert _noalloc(lib, layer, n=-1) == -9
+    assert _noalloc(lib, _layer(head_dim=128), n=too_many) == -3
+    assert _noalloc(lib, layer, n=too_many) == -16
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
+def test_noalloc_without_gpu_fails_loudly(lib):
+    """Valid arguments on a host without a GPU: the one-time address lookup
+    cannot run, and nothing falls back to the CPU."""
+    assert _noalloc(lib, _layer(), n=0) == -13
+    assert _noalloc(lib, _layer(), n=4) == -13

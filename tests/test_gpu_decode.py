@@ -54,14 +54,12 @@ def test_sliding_decode_batch_full_size(orc):
     run_decode(orc, wl.sliding_decode().steps[0], check_pools=False)
 
 
-def test_full_keqv_decode_full_size_sampled(orc):
-    step = wl.full_keqv_decode().steps[0]
-    lens = step.seq_lens
-    rng = np.random.default_rng(0)
-    seqs = sorted(set([int(np.argmin(lens)), int(np.argmax(lens))] +
-                      rng.choice(len(lens), 6, replace=False).tolist()))
-    g = run_decode(orc, step, seqs=seqs, check_pools=False)
+def test_full_keqv_decode_full_size(orc):
+    """Every sequence of the full-layer k_eq_v batch (32 sequences up to 32768
+    keys, head_dim 512, V read from the K pages)."""
+    g = run_decode(orc, wl.full_keqv_decode().steps[0], check_pools=False)
     assert torch.isfinite(g.out).all() and torch.isfinite(g.lse).all()
+    assert not g.ws[:binding.WORKSPACE_COUNTER_BYTES].any(), "merge tickets left non-zero"
 
 
 EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 47, 48, 49, 63, 64, 65, 79, 80, 81, 127, 128, 129,
@@ -75,6 +73,9 @@ EDGE_LAYERS = [
     pytest.param(Layer(8, 2, 512, window=48), id="hd512-g4-w48"),
     pytest.param(Layer(4, 4, 256, window=0, k_eq_v=True, scale=0.5), id="hd256-g1-keqv"),
     pytest.param(Layer(12, 4, 256, window=33), id="hd256-g3-w33"),
+    pytest.param(Layer(32, 4, 512, window=0, k_eq_v=True, softcap=30.0, scale=0.0625),
+                 id="hd512-g8-keqv-cap"),
+    pytest.param(Layer(16, 2, 512, window=200, softcap=20.0), id="hd512-g8-w200-cap"),
 ]
 
 
@@ -86,12 +87,56 @@ def test_decode_edge_lengths(orc, layer):
 
 
 def test_decode_many_sequences_split_units(orc):
-    """More tiles than CTAs: units are cut across CTAs and merged."""
+    """More tiles than CTAs: units are cut across CTAs and merged; the merge
+    tickets are back at zero afterwards."""
     rng = np.random.default_rng(3)
     lens = rng.integers(1, 3000, size=300)
     step = wl.custom_step(Layer(16, 8, 256, window=1024), 11, lens - 1, np.ones_like(lens),
                           threads=8)
-    run_decode(orc, step, check_pools=False)
+    g = run_decode(orc, step, check_pools=False)
+    assert not g.ws[:binding.WORKSPACE_COUNTER_BYTES].any(), "merge tickets left non-zero"
+
+
+def test_decode_workspace_reused_by_smaller_then_larger_batches(orc):
+    """One zero-filled workspace serves calls of different batch sizes in a
+    row (tickets left at zero by each call)."""
+    layer = Layer(16, 8, 256, window=512, softcap=40.0)
+    rng = np.random.default_rng(17)
+    big = rng.integers(1, 2500, size=200)
+    small = rng.integers(1, 6000, size=7)
+    steps = [wl.custom_step(layer, 18 + i, lens - 1, np.ones_like(lens), threads=8)
+             for i, lens in enumerate((big, small, big))]
+    ws = binding.alloc_workspace(layer, 200, 6000)
+    for step in steps:
+        g = GpuStep(step)
+        g.ws = ws
+        g.write_new()
+        g.decode()
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        o = OracleStep(orc, step)
+        ref_out, ref_lse = o.decode()
+        assert_close(g.out.cpu().numpy(), ref_out, "decode out")
+        assert_close(g.lse.cpu().numpy(), ref_lse, "decode lse")
+        assert not ws[:binding.WORKSPACE_COUNTER_BYTES].any(), "merge tickets left non-zero"
+
+
+def test_decode_without_lse(orc):
+    """lse = NULL: the output alone is written, identical to a call with lse."""
+    step = wl.custom_step(Layer(32, 4, 512, window=0, k_eq_v=True), 19,
+                          np.array([20000, 5, 700]), np.ones(3, np.int64), threads=8)
+    g = GpuStep(step)
+    g.write_new()
+    g.decode()
+    with_lse = g.out.clone()
+    out = torch.full_like(g.out, float("nan"))
+    binding.attn_decode_paged(step.layer, g.q, g.k_pool, g.v_pool, g.pages, g.seq_lens, out,
+                              None, g.ws)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert torch.equal(out, with_lse)
+    ref_out, _ = OracleStep(orc, step).decode()
+    assert_close(out.cpu().numpy(), ref_out, "decode out (lse NULL)")
 
 
 def test_decode_single_long_sequence(orc):

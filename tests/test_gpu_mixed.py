@@ -2,9 +2,9 @@
 layers, then 1 full hd512 k_eq_v layer; 256 decode sequences plus 4 prefill
 chunks of 2048 tokens): every layer runs kv_cache_write, attn_decode_paged and
 attn_prefill_chunked through the C ABI. Outputs are compared with the oracle on
-every decode row of the sliding layers, sampled decode rows of the full layer
-and sampled prefill rows (the whole step is too large for an fp64 CPU pass);
-every output is checked finite."""
+every decode row of every layer and on sampled prefill rows (all prefill rows
+are about 4 TFLOP of fp64 work, too much for a CPU pass); every output is
+checked finite."""
 import numpy as np
 import pytest
 import torch
@@ -38,7 +38,6 @@ def test_mixed_hybrid_step_all_layers():
     orc = oracle.default()
     work = wl.mixed_hybrid(threads=16)
     nd = work.decode_seqs
-    rng = np.random.default_rng(5)
     for li, step in enumerate(work.steps):
         m = MixedLayerStep(step, nd)
         m.run()
@@ -46,6 +45,7 @@ def test_mixed_hybrid_step_all_layers():
         assert binding.get_error() == 0, f"layer {li}: device error"
         g = m.g
         assert torch.isfinite(g.out).all() and torch.isfinite(g.lse).all(), f"layer {li}"
+        assert not g.ws[:binding.WORKSPACE_COUNTER_BYTES].any(), f"layer {li}: tickets"
         got_out = g.out.cpu().numpy()
         got_lse = g.lse.cpu().numpy()
         # oracle pools for this layer, written in place
@@ -57,12 +57,9 @@ def test_mixed_hybrid_step_all_layers():
                            step.block_table, kp, vp, in_place=True)
         L = step.layer.as_dict()
         lens = step.seq_lens[:nd]
-        # every decode row of a sliding layer (at most W keys each); for the
-        # full layer, whose rows reach 65536 keys, the shortest, the longest
-        # and 12 seeded ones
-        sample = sorted(set(rng.choice(nd, 12, replace=False).tolist() +
-                            [int(np.argmax(lens)), int(np.argmin(lens))]))
-        seqs = list(range(nd)) if step.layer.window > 0 else sample
+        # every decode row of every layer (the full layer's rows reach 65536
+        # keys: about 25 G multiply-adds of fp64 oracle work)
+        seqs = list(range(nd))
         ref_o, ref_l, _ = orc.decode(L, step.q[:nd], kp, vp, step.block_table[:nd], lens,
                                      seqs=seqs)
         # decode rows are the first nd rows of q/out (one new token each)

@@ -59,10 +59,13 @@ def run_prefill(orc, step, rows=None, check_pools=True):
     return g
 
 
-def test_chunked_prefill_softcap_full_size_sampled(orc):
+def test_chunked_prefill_softcap_full_size(orc):
+    """Every row of the chunked-prefill workload (8 chunks of 512 tokens after
+    0-8192 cached ones, window 1024, softcap 50) against the oracle."""
     step = wl.chunked_prefill().steps[0]
-    g = run_prefill(orc, step, rows=sample_rows(step))
+    g = run_prefill(orc, step)
     assert torch.isfinite(g.out).all() and torch.isfinite(g.lse).all()
+    assert not g.ws[:binding.WORKSPACE_COUNTER_BYTES].any(), "counter block written"
 
 
 PREFILL_CASES = [
@@ -82,6 +85,11 @@ PREFILL_CASES = [
                  [130, 64, 70], id="hd512-g8-w100-keqv-cap"),
     pytest.param(Layer(4, 4, 256, window=0, k_eq_v=True), [0, 31], [31, 66], id="hd256-g1-keqv"),
     pytest.param(Layer(12, 4, 256, window=33), [0, 50], [45, 20], id="hd256-g3-w33"),
+    # empty chunks between (and after) non-empty ones: cu_q[b + 1] == cu_q[b]
+    pytest.param(Layer(8, 4, 256, window=64, softcap=50.0, scale=0.0625),
+                 [100, 40, 0, 300, 7], [70, 0, 65, 0, 0], id="hd256-g2-empty-chunks"),
+    pytest.param(Layer(32, 4, 512, window=0, k_eq_v=True), [0, 500, 33], [0, 40, 129],
+                 id="hd512-g8-keqv-empty-first"),
 ]
 
 
@@ -178,3 +186,22 @@ def test_decode_rescale_after_low_first_maximum(orc):
     ref_out, ref_lse = OracleStep(orc, step).decode()
     assert_close(g.out.cpu().numpy(), ref_out, "decode out")
     assert_close(g.lse.cpu().numpy(), ref_lse, "decode lse")
+
+
+def test_prefill_without_lse(orc):
+    """lse = NULL: the output alone is written, identical to a call with lse."""
+    layer = Layer(16, 2, 512, window=100, k_eq_v=True, softcap=30.0)
+    step = wl.custom_step(layer, 71, [0, 300, 1000], [130, 64, 70])
+    g = GpuStep(step)
+    g.write_new()
+    g.prefill()
+    with_lse = g.out.clone()
+    out = torch.full_like(g.out, float("nan"))
+    max_q = int(step.new_lens.max())
+    binding.attn_prefill_chunked(layer, g.q, g.cu_new, g.past, max_q, g.k_pool, g.v_pool,
+                                 g.pages, out, None, g.ws)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert torch.equal(out, with_lse)
+    ref_out, _ = OracleStep(orc, step).prefill()
+    assert_close(out.cpu().numpy(), ref_out, "prefill out (lse NULL)")
