@@ -5,7 +5,7 @@ One step = the serving step of one sliding attention layer over the
 sliding-layer decode batch (64 sequences, lengths uniform in [512, 4096],
 head_dim 256, 16 query / 8 KV heads, window 1024, 16-token pages in a pool of
 32768 blocks): kv_cache_write of the step's new K/V rows, then
-attn_decode_paged (device plan, split-KV kernel, LSE merge).
+attn_decode_paged (one split-KV kernel launch that also merges).
 
 Metric: decode attention KV-read GB/s = algorithmic K+V bytes the step must
 read (sum over sequences of min(len, W) keys x n_kv x head_dim x 2 B x 2)
@@ -775,9 +775,12 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(step),
-        "roofline": {"bound": "hbm", "kernel": "attn_decode_paged (plan + split + merge)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_split_kernel<256, false> (attn_decode_paged: one launch)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": traffic},
+                     "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": traffic,
+                     "traffic_source": "committed ncu summary (DRAM read + write per launch),"
+                                       " null once the kernel source changed"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
