@@ -39,6 +39,7 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_f32p = ctypes.POINTER(ctypes.c_float)
 
 
 def compile_source(src_path: str, lib_path: str) -> str:
@@ -83,6 +84,17 @@ class Oracle:
             _u16p, _u16p]
         lib.oracle_num_cores.restype = ctypes.c_int32
         lib.oracle_num_cores.argtypes = []
+        lib.oracle_norm_rope_row.restype = None
+        lib.oracle_norm_rope_row.argtypes = [
+            _u16p, ctypes.c_int32, ctypes.c_double, _f32p, ctypes.c_int32, ctypes.c_double,
+            ctypes.c_int32, ctypes.c_int64, _f64p]
+        lib.oracle_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_qkv_norm_rope.restype = None
+        lib.oracle_qkv_norm_rope.argtypes = [
+            _u16p, _u16p, _u16p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_double, _f32p, _f32p, _f32p, ctypes.c_double,
+            ctypes.c_int32, _f64p, _f64p, _f64p]
         lib.oracle_attention_rows.restype = ctypes.c_int32
         lib.oracle_attention_rows.argtypes = [
             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -190,6 +202,54 @@ class Oracle:
                                    k_pool, v_pool, block_table, threads)
 
 
+    # ---------------------------------------------------------- pre-attention step
+    def norm_rope_row(self, x, eps: float, weight=None, rotate: bool = True,
+                      theta: float = 10000.0, rope_angles: int | None = None, pos: int = 0):
+        """One head vector (bf16 bits): RMS-norm (optional weight), then the
+        proportional rotary embedding at ``pos`` when ``rotate``. fp64 out."""
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        hd = x.shape[-1]
+        ra = hd // 2 if rope_angles is None else int(rope_angles)
+        w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float32)
+        out = np.zeros(hd, dtype=np.float64)
+        self.lib.oracle_norm_rope_row(_ptr(x, ctypes.c_uint16), hd, float(eps),
+                                      _ptr(w, ctypes.c_float), int(bool(rotate)), float(theta),
+                                      ra, int(pos), _ptr(out, ctypes.c_double))
+        return out
+
+    def qkv_norm_rope(self, q, k, v, cu_new, past_lens, eps: float, theta: float,
+                      rope_angles: int, q_w=None, k_w=None, v_w=None):
+        """The pre-attention step of one layer: returns (q_out, k_rows, v_rows)
+        in fp64 (k_rows / v_rows None when k / v is None)."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        n_tok, n_q, hd = q.shape
+        cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
+        past_lens = np.ascontiguousarray(past_lens, dtype=np.int32)
+        k = None if k is None else np.ascontiguousarray(k, dtype=np.uint16)
+        v = None if v is None else np.ascontiguousarray(v, dtype=np.uint16)
+        n_kv = k.shape[1] if k is not None else (v.shape[1] if v is not None else 1)
+        ws = [None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+              for w in (q_w, k_w, v_w)]
+        q_out = np.zeros((n_tok, n_q, hd), dtype=np.float64)
+        k_rows = None if k is None else np.zeros((n_tok, n_kv, hd), dtype=np.float64)
+        v_rows = None if v is None else np.zeros((n_tok, n_kv, hd), dtype=np.float64)
+        self.lib.oracle_qkv_norm_rope(
+            _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+            _ptr(cu_new, ctypes.c_int32), _ptr(past_lens, ctypes.c_int32),
+            past_lens.shape[0], n_q, n_kv, hd, float(eps),
+            _ptr(ws[0], ctypes.c_float), _ptr(ws[1], ctypes.c_float),
+            _ptr(ws[2], ctypes.c_float), float(theta), int(rope_angles),
+            _ptr(q_out, ctypes.c_double), _ptr(k_rows, ctypes.c_double),
+            _ptr(v_rows, ctypes.c_double))
+        return q_out, k_rows, v_rows
+
+    def to_bf16(self, values) -> np.ndarray:
+        """Round fp64 values to bf16 bits (nearest, ties to even)."""
+        a = np.asarray(values, dtype=np.float64)
+        f = np.frompyfunc(lambda x: int(self.lib.oracle_to_bf16(float(x))), 1, 1)
+        return f(a).astype(np.uint16).reshape(a.shape)
+
+
 def default() -> Oracle:
     """The oracle built from psw_oracle.c (compiled on first use)."""
     global _default
@@ -225,3 +285,15 @@ def decode(*args, **kw):
 
 def prefill(*args, **kw):
     return default().prefill(*args, **kw)
+
+
+def norm_rope_row(*args, **kw):
+    return default().norm_rope_row(*args, **kw)
+
+
+def qkv_norm_rope(*args, **kw):
+    return default().qkv_norm_rope(*args, **kw)
+
+
+def to_bf16(values):
+    return default().to_bf16(values)

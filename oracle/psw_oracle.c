@@ -33,6 +33,8 @@
  *  - KV-cache size: batch * seq * layers * n_kv * head_dim * bytes, doubled
  *    when a separate V cache is kept (the KV-size worked example in
  *    "Gemma 4 architecture decoded", GQA section).
+ *  - The pre-attention step: per-head RMS-norm of q, k and v, then the
+ *    proportional rotary embedding of q and k (see oracle_norm_rope_row).
  *
  * Arithmetic: bf16 inputs are widened exactly to double; every sum, the
  * softcap, the exponentials and the normalisation run in double.
@@ -293,4 +295,114 @@ int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
     free(jobs);
     free(threads);
     return failed ? -2 : n_threads;
+}
+
+/*
+ * ---- pre-attention step: RMS-norm of q/k/v head vectors, proportional RoPE
+ *
+ * Per head vector x of length hd (all arithmetic in double):
+ *   y_d = x_d / sqrt(mean_e(x_e^2) + eps) * w_d      (w_d = 1 when no weight)
+ * (RMSNorm per head vector before RoPE: InfiniLM PR 581, Gemma-3 item 1; the
+ * weights are the effective ones, the checkpoint's zero-centred w plus 1,
+ * as that item's remapper loads them; v_norm: "MNN supports the full Gemma4
+ * family", section 6.1.)
+ * Then, for q and k only (V is not rotated: same page, section 6.2), the
+ * proportional rotary embedding of "Gemma 4 model architecture analysis",
+ * challenge 5: frequency i of the hd/2 pairs is theta^(-2i/hd) for
+ * i < rope_angles and 0 beyond (the zero-padded, unrotated dims), so the
+ * exponent's denominator is the head size, not the rotated size. Pair i
+ * couples dims i and i + hd/2 (rotate-half form):
+ *   out_i        = y_i cos(a_i) - y_{i+hd/2} sin(a_i)
+ *   out_{i+hd/2} = y_{i+hd/2} cos(a_i) + y_i sin(a_i),   a_i = pos * freq_i
+ */
+void oracle_norm_rope_row(const uint16_t *x, int32_t hd, double eps,
+                          const float *weight, int32_t rotate, double theta,
+                          int32_t rope_angles, int64_t pos, double *out)
+{
+    double ss = 0.0;
+    for (int32_t d = 0; d < hd; ++d) {
+        double v = bf16_bits_to_double(x[d]);
+        ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / (double)hd + eps);
+    double *y = out; /* normalised in place, then rotated pair by pair */
+    for (int32_t d = 0; d < hd; ++d)
+        y[d] = bf16_bits_to_double(x[d]) * inv *
+               (weight != NULL ? (double)weight[d] : 1.0);
+    if (!rotate)
+        return;
+    int32_t half = hd / 2;
+    for (int32_t i = 0; i < half; ++i) {
+        double freq = (i < rope_angles)
+                          ? pow(theta, -2.0 * (double)i / (double)hd)
+                          : 0.0;
+        double a = (double)pos * freq;
+        double c = cos(a), s = sin(a);
+        double lo = y[i], hi = y[i + half];
+        y[i] = lo * c - hi * s;
+        y[i + half] = hi * c + lo * s;
+    }
+}
+
+/* Round a double to the nearest bf16 (ties to even); returns its bits. */
+uint16_t oracle_to_bf16(double v)
+{
+    if (v != v)
+        return 0x7FC0;
+    int neg = signbit(v) != 0;
+    double a = fabs(v);
+    uint16_t sign = neg ? 0x8000 : 0;
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e, 0.5 <= f < 1 */
+    /* quantum of a bf16 with this exponent (8 significant bits), never
+       finer than the smallest subnormal 2^-133 */
+    int qexp = e - 8;
+    if (qexp < -133)
+        qexp = -133;
+    double n = nearbyint(ldexp(a, -qexp)); /* default rounding: ties to even */
+    double r = ldexp(n, qexp);
+    if (r > 3.3895313892515355e38) /* beyond the largest finite bf16 */
+        return sign | 0x7F80;
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+/*
+ * The whole pre-attention step of one layer for the new tokens of a batch:
+ * token t of sequence b sits at position past_lens[b] + (t - cu_new[b]).
+ * q_out[t][h] = rope(norm_q(q[t][h])); when k_rows is non-NULL (a layer that
+ * owns its cache) k_rows[t][g] = rope(norm_k(k[t][g])) and, when v_rows is
+ * non-NULL, v_rows[t][g] = norm_v(v[t][g]) (no rotation). Outputs in double;
+ * writing them into pages is oracle_kv_cache_write's job, after rounding.
+ */
+void oracle_qkv_norm_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *cu_new, const int32_t *past_lens,
+                          int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads,
+                          int32_t hd, double eps, const float *q_w, const float *k_w,
+                          const float *v_w, double theta, int32_t rope_angles,
+                          double *q_out, double *k_rows, double *v_rows)
+{
+    for (int32_t b = 0; b < n_seqs; ++b) {
+        for (int32_t t = cu_new[b]; t < cu_new[b + 1]; ++t) {
+            int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]);
+            for (int32_t h = 0; h < n_q_heads; ++h) {
+                int64_t o = ((int64_t)t * n_q_heads + h) * hd;
+                oracle_norm_rope_row(q + o, hd, eps, q_w, 1, theta, rope_angles, pos,
+                                     q_out + o);
+            }
+            for (int32_t g = 0; g < n_kv_heads; ++g) {
+                int64_t o = ((int64_t)t * n_kv_heads + g) * hd;
+                if (k_rows != NULL)
+                    oracle_norm_rope_row(k + o, hd, eps, k_w, 1, theta, rope_angles,
+                                         pos, k_rows + o);
+                if (v_rows != NULL)
+                    oracle_norm_rope_row(v + o, hd, eps, v_w, 0, theta, rope_angles,
+                                         pos, v_rows + o);
+            }
+        }
+    }
 }

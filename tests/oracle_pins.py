@@ -24,6 +24,7 @@ import os
 
 import numpy as np
 
+from oracle_pins_rope import ROPE_CHECKS
 from paged_sliding_window_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -460,4 +461,4 @@ ALL_CHECKS = [
     check_gqa_grouping, check_empty_sequence, check_paged_equals_contiguous,
     check_decode_equals_last_prefill_row, check_prefill_equals_sequential_decodes,
     check_softcap_to_identity, check_k_eq_v_equals_copy,
-]
+] + ROPE_CHECKS

@@ -27,6 +27,23 @@ MUTANTS = [
     ("cache write skips v", "memcpy(v_pool + slot * row_elems",
      "if (0) memcpy(v_pool + slot * row_elems"),
     ("kv size missing v factor", "return with_v ? 2.0 * one : one;", "return one;"),
+    ("rope denominator is the rotated size", "pow(theta, -2.0 * (double)i / (double)hd)",
+     "pow(theta, -2.0 * (double)i / (double)(2 * rope_angles))"),
+    ("rope sin sign", "y[i] = lo * c - hi * s;", "y[i] = lo * c + hi * s;"),
+    ("rope rotates the unrotated dims", "double freq = (i < rope_angles)",
+     "double freq = (1)"),
+    ("rope adjacent pairs", "double lo = y[i], hi = y[i + half];",
+     "double lo = y[i], hi = y[(i + 1) % hd];"),
+    ("v rotated", "oracle_norm_rope_row(v + o, hd, eps, v_w, 0,",
+     "oracle_norm_rope_row(v + o, hd, eps, v_w, 1,"),
+    ("norm eps outside the root", "1.0 / sqrt(ss / (double)hd + eps)",
+     "1.0 / (sqrt(ss / (double)hd) + eps)"),
+    ("norm over the sum", "1.0 / sqrt(ss / (double)hd + eps)", "1.0 / sqrt(ss + eps)"),
+    ("norm weight ignored", "(weight != NULL ? (double)weight[d] : 1.0)", "1.0"),
+    ("rope position off by one", "int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]);\n            for (int32_t h",
+     "int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]) + 1;\n            for (int32_t h"),
+    ("bf16 rounding truncates", "double n = nearbyint(ldexp(a, -qexp));",
+     "double n = floor(ldexp(a, -qexp));"),
 ]
 
 
