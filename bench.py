@@ -479,6 +479,42 @@ def measure_full_decode(steps, warmup, hbm, peak_kind):
             "gpu_launches_per_call": 1}
 
 
+def measure_pre_attention(steps, warmup, hbm, peak_kind):
+    """The fused pre-attention step (per-head RMS-norm, proportional RoPE,
+    cache write) over the chunked-prefill workload's 4096 new tokens and over
+    the sliding decode batch's 64: GB/s of the bytes it must move (q, k, v
+    read; q_out, K and V rows written), L2 flushed before every call."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+    from paged_sliding_window_gb300.staging import GpuStep, dev_bf16
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    res = {}
+    for name, theta in (("chunked_prefill", 1e4), ("sliding_decode", 1e4)):
+        step = first_step(name)
+        L = step.layer
+        g = GpuStep(step)
+        rn = binding.make_norm_rope(theta, 1.0, 1e-6)
+        q_out = torch.empty_like(g.q)
+
+        def call():
+            binding.qkv_norm_rope_cache_write(L, rn, g.q, g.new_k, g.new_v, g.cu_new, g.past,
+                                              g.pages, q_out, g.k_pool, g.v_pool)
+        ms = time_calls(call, steps, warmup, lambda: flush_l2(scratch))
+        assert binding.get_error() == 0
+        n_tok = int(step.cu_new[-1])
+        nbytes = 2 * n_tok * (L.n_q_heads + 2 * L.n_kv_heads) * L.head_dim * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"tokens": n_tok, "ms_per_call": ms, "bytes_per_call": nbytes,
+                     "value": gbs, "unit": "GB/s",
+                     "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_kernel<256>",
+                                  "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                  "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": None}}
+        del g
+    return {"workload": "fused pre-attention step (q/k/v RMS-norm, RoPE, cache write)",
+            "l2": "flushed (256 MB write) before every timed call", **res,
+            "gpu_launches_per_call": 1}
+
+
 def decode_kv_bytes_subset(step: wl.Step, n: int) -> int:
     L = step.layer
     lens = step.seq_lens[:n].astype(np.int64)
@@ -791,6 +827,8 @@ def main():
         hbm_p, tf_p, kind_p, _ = peaks()
         line["prefill"] = measure_prefill(args.steps, args.warmup, tf_p, kind_p)
         line["full_keqv_decode"] = measure_full_decode(args.steps, args.warmup, hbm_p, kind_p)
+        line["pre_attention_step"] = measure_pre_attention(args.steps, args.warmup, hbm_p,
+                                                           kind_p)
         if not args.no_mixed:
             line["mixed_hybrid_step"] = measure_mixed(min(args.steps, 10), 3)
     if rank == 0 and world == 1 and args.cpu_budget > 0:

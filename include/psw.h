@@ -85,6 +85,10 @@ typedef struct CUstream_st *psw_stream_t;
 #define PSW_ETENSORMAP       -15  /* the TMA descriptor for a pool could not be built */
 #define PSW_ESCRATCH         -16  /* the batch needs more scratch than the static buffer of
                                      attn_decode_paged_noalloc holds */
+#define PSW_EINVAL_ROPE      -17  /* theta <= 0, partial_rotary_factor outside (0, 1], eps < 0,
+                                     or one of them not finite */
+#define PSW_EINVAL_LAYERS    -18  /* n_layers or pattern <= 0, n_shared outside [0, n_layers),
+                                     or a shared layer with no cache-owning layer of its type */
 
 /* ---- device error bits (psw_get_error) ---- */
 #define PSW_DEVERR_BLOCK_ID    1  /* block id outside [0, num_blocks): access skipped */
@@ -237,6 +241,77 @@ PSW_API int attn_decode_paged_noalloc(const psw_layer_t *layer, const void *q,
                                       const psw_pages_t *pages, const int32_t *seq_lens,
                                       int32_t n_seqs, float *out, float *lse,
                                       psw_stream_t stream);
+
+/* Parameters of the pre-attention step of one layer. */
+typedef struct {
+  float theta;                  /* RoPE base: 10000 on sliding layers, 1e6 on full layers */
+  float partial_rotary_factor;  /* fraction of head_dim that is rotated, in (0, 1] */
+  float eps;                    /* RMS-norm epsilon, >= 0 */
+  const float *q_weight;        /* device fp32 [head_dim]: effective q_norm weight, or NULL */
+  const float *k_weight;        /* device fp32 [head_dim]: effective k_norm weight, or NULL */
+  const float *v_weight;        /* device fp32 [head_dim]: v_norm weight, or NULL (weightless) */
+} psw_norm_rope_t;
+
+/*
+ * The step before attention, fused into one kernel: per-head RMS-norm of the
+ * new tokens' q, k and v, the proportional rotary embedding of q and k, and
+ * the cache write of k and v.
+ *
+ * Per head vector x (head_dim elements) of token t of sequence b, at position
+ * pos = past_lens[b] + (t - cu_new[b]):
+ *   y_d = x_d / sqrt(mean(x^2) + eps) * w_d        (w_d = 1 without a weight)
+ * (RMS-norm per head vector before the rotation: InfiniLM PR 581, Gemma-3
+ * item 1, whose weights are stored as w - 1 and loaded as w: pass the loaded
+ * weight; v_norm: "MNN supports the full Gemma4 family", section 6.1). For q
+ * and k only (V is not rotated, same page section 6.2), the proportional
+ * rotary embedding of "Gemma 4 model architecture analysis", challenge 5:
+ * with rope_angles = floor(partial_rotary_factor * head_dim / 2), pair i of
+ * dims (i, i + head_dim / 2) turns by a = pos * theta^(-2 i / head_dim) for
+ * i < rope_angles (the head size, not the rotated size, is the exponent's
+ * denominator) and not at all beyond:
+ *   out_i = y_i cos a - y_{i + hd/2} sin a,  out_{i + hd/2} = y_{i + hd/2} cos a + y_i sin a.
+ * The rotate-half pairing is this library's reading; the pages do not print
+ * the pairing. Results are rounded to bf16 (nearest, ties to even):
+ *   q_out  device bf16 [n_new_total][n_q_heads][head_dim]; may be q itself
+ *   k_pool, v_pool  receive the rotated k and the normalised v rows in the
+ *          slot block_table[b][pos / 16] * 16 + pos % 16, as kv_cache_write
+ * Inputs: q device bf16 [n_new_total][n_q_heads][head_dim]; k, v device bf16
+ * [n_new_total][n_kv_heads][head_dim]; cu_new, past_lens as kv_cache_write.
+ * A layer whose V aliases its K pages (k_eq_v) passes v = v_pool = NULL. A
+ * Gemma-4 layer whose V comes from the K projection (different from K: only
+ * normalised) is a k_eq_v = 0 layer that passes the same raw k buffer as v.
+ * A layer that reads another layer's cache (KV sharing) passes k = v =
+ * k_pool = v_pool = NULL (and may pass pages = NULL): only q is processed.
+ * Errors: those of kv_cache_write, PSW_EINVAL_ROPE, and PSW_ENULL for a
+ * missing rn, q or q_out. Device-side errors (block id, capacity, lengths)
+ * are flagged as by kv_cache_write; q_out is still written for such tokens.
+ */
+PSW_API int qkv_norm_rope_cache_write(const psw_layer_t *layer, const psw_norm_rope_t *rn,
+                                      const void *q, const void *k, const void *v,
+                                      const int32_t *cu_new, const int32_t *past_lens,
+                                      int32_t n_seqs, const psw_pages_t *pages, void *q_out,
+                                      void *k_pool, void *v_pool, psw_stream_t stream);
+
+/*
+ * Layer types of a hybrid stack and its KV-sharing map. Host arithmetic only
+ * (no GPU, nothing launched).
+ *   is_full[i] = 1 when (i + 1) % pattern == 0, else 0 (sliding): the
+ *     interleaving rule of InfiniLM PR 581, Gemma-3 item 2 (pattern 6 gives
+ *     Gemma-3's 5:1 stack).
+ *   target[i]  = i for the first n_layers - n_shared layers, which own their
+ *     caches; each of the last n_shared layers reads the cache of the last
+ *     cache-owning layer of its own type and writes none ("MNN supports the
+ *     full Gemma4 family", KV-sharing section: in the 35-layer E2B with
+ *     pattern 5 and 20 shared layers, sliding layers read layer 13 and full
+ *     layers read layer 14; "Gemma 4 model architecture analysis", section 4:
+ *     a shared layer keeps its own q projection, skips the cache write and
+ *     attends over its target's pages).
+ * A shared layer runs qkv_norm_rope_cache_write with k = v = NULL and then
+ * the attention calls on its target's pools and block table.
+ * Either output pointer may be NULL. Returns PSW_OK or PSW_EINVAL_LAYERS.
+ */
+PSW_API int psw_kv_share_map(int32_t n_layers, int32_t pattern, int32_t n_shared,
+                             int32_t *is_full, int32_t *target);
 
 /*
  * Synchronises `stream`, then returns the current device's error word (an OR

@@ -90,6 +90,8 @@ class Oracle:
             ctypes.c_int32, ctypes.c_int64, _f64p]
         lib.oracle_to_bf16.restype = ctypes.c_uint16
         lib.oracle_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_to_bf16_array.restype = None
+        lib.oracle_to_bf16_array.argtypes = [_f64p, _u16p, ctypes.c_int64]
         lib.oracle_qkv_norm_rope.restype = None
         lib.oracle_qkv_norm_rope.argtypes = [
             _u16p, _u16p, _u16p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -245,9 +247,11 @@ class Oracle:
 
     def to_bf16(self, values) -> np.ndarray:
         """Round fp64 values to bf16 bits (nearest, ties to even)."""
-        a = np.asarray(values, dtype=np.float64)
-        f = np.frompyfunc(lambda x: int(self.lib.oracle_to_bf16(float(x))), 1, 1)
-        return f(a).astype(np.uint16).reshape(a.shape)
+        a = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(a.shape, dtype=np.uint16)
+        self.lib.oracle_to_bf16_array(_ptr(a, ctypes.c_double), _ptr(out, ctypes.c_uint16),
+                                      a.size)
+        return out
 
 
 def default() -> Oracle:

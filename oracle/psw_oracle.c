@@ -406,3 +406,10 @@ void oracle_qkv_norm_rope(const uint16_t *q, const uint16_t *k, const uint16_t *
         }
     }
 }
+
+/* oracle_to_bf16 over an array. */
+void oracle_to_bf16_array(const double *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_to_bf16(v[i]);
+}

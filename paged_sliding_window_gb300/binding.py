@@ -22,12 +22,13 @@ ERRORS = {
     -5: "PSW_EINVAL_WINDOW", -6: "PSW_EINVAL_BLOCKSIZE", -7: "PSW_EINVAL_KEQV",
     -8: "PSW_EINVAL_SCALE", -9: "PSW_EINVAL_NSEQS", -10: "PSW_EWORKSPACE",
     -11: "PSW_ECAPACITY", -12: "PSW_EALIGN", -13: "PSW_EDEVICE", -14: "PSW_ELAUNCH",
-    -15: "PSW_ETENSORMAP", -16: "PSW_ESCRATCH",
+    -15: "PSW_ETENSORMAP", -16: "PSW_ESCRATCH", -17: "PSW_EINVAL_ROPE",
+    -18: "PSW_EINVAL_LAYERS",
 }
 DEVERR_BLOCK_ID, DEVERR_CAPACITY, DEVERR_LENGTH, DEVERR_PIPELINE = 1, 2, 4, 8
 EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
             "attn_prefill_chunked", "psw_get_error", "psw_strerror",
-            "attn_decode_paged_noalloc")
+            "attn_decode_paged_noalloc", "qkv_norm_rope_cache_write", "psw_kv_share_map")
 
 
 class PswLayer(ctypes.Structure):
@@ -40,6 +41,12 @@ class PswLayer(ctypes.Structure):
 class PswPages(ctypes.Structure):
     _fields_ = [("block_table", ctypes.c_void_p), ("max_blocks_per_seq", ctypes.c_int32),
                 ("num_blocks", ctypes.c_int64)]
+
+
+class PswNormRope(ctypes.Structure):
+    _fields_ = [("theta", ctypes.c_float), ("partial_rotary_factor", ctypes.c_float),
+                ("eps", ctypes.c_float), ("q_weight", ctypes.c_void_p),
+                ("k_weight", ctypes.c_void_p), ("v_weight", ctypes.c_void_p)]
 
 
 class PswError(RuntimeError):
@@ -78,6 +85,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                              vp, sz, vp]
         lib.attn_decode_paged_noalloc.argtypes = [lp, vp, vp, vp, pp, vp, i32, vp, vp, vp]
         lib.attn_decode_paged_noalloc.restype = ctypes.c_int
+        lib.qkv_norm_rope_cache_write.argtypes = [lp, ctypes.POINTER(PswNormRope), vp, vp, vp,
+                                                  vp, vp, i32, pp, vp, vp, vp, vp]
+        lib.qkv_norm_rope_cache_write.restype = ctypes.c_int
+        lib.psw_kv_share_map.argtypes = [i32, i32, i32, ctypes.POINTER(i32),
+                                         ctypes.POINTER(i32)]
+        lib.psw_kv_share_map.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.psw_strerror.argtypes = [ctypes.c_int]
         lib.psw_strerror.restype = ctypes.c_char_p
@@ -212,6 +225,46 @@ def attn_decode_paged_noalloc(layer, q, k_pool, v_pool, pages: PswPages, seq_len
                                           _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(out),
                                           _ptr(lse), _stream(stream))
     _raise(rc, "attn_decode_paged_noalloc")
+
+
+def make_norm_rope(theta: float, partial_rotary_factor: float = 1.0, eps: float = 1e-6,
+                   q_weight=None, k_weight=None, v_weight=None) -> PswNormRope:
+    """psw_norm_rope_t from device fp32 weight tensors (or None)."""
+    for t, n in ((q_weight, "q_weight"), (k_weight, "k_weight"), (v_weight, "v_weight")):
+        _check(t, torch.float32, n)
+    return PswNormRope(float(theta), float(partial_rotary_factor), float(eps),
+                       None if q_weight is None else q_weight.data_ptr(),
+                       None if k_weight is None else k_weight.data_ptr(),
+                       None if v_weight is None else v_weight.data_ptr())
+
+
+def qkv_norm_rope_cache_write(layer, rn: PswNormRope, q, k, v, cu_new, past_lens,
+                              pages: PswPages | None, q_out, k_pool, v_pool,
+                              stream=None) -> None:
+    """The fused pre-attention step (per-head RMS-norm, proportional RoPE of q
+    and k, cache write of k and v). k = v = pools = None processes q only."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (q_out, "q_out"), (k_pool, "k_pool"),
+                 (v_pool, "v_pool")):
+        _check(t, torch.bfloat16, n)
+    _check(cu_new, torch.int32, "cu_new")
+    _check(past_lens, torch.int32, "past_lens")
+    rc = load().qkv_norm_rope_cache_write(
+        ctypes.byref(make_layer(layer)), ctypes.byref(rn), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(cu_new), _ptr(past_lens), int(past_lens.shape[0]),
+        None if pages is None else ctypes.byref(pages), _ptr(q_out), _ptr(k_pool), _ptr(v_pool),
+        _stream(stream))
+    _raise(rc, "qkv_norm_rope_cache_write")
+
+
+def kv_share_map(n_layers: int, pattern: int, n_shared: int = 0):
+    """(is_full, target) lists of a hybrid stack (psw_kv_share_map): layer i is
+    full when (i + 1) % pattern == 0; the last n_shared layers read the cache of
+    the last cache-owning layer of their type."""
+    full = (ctypes.c_int32 * n_layers)()
+    tgt = (ctypes.c_int32 * n_layers)()
+    _raise(load().psw_kv_share_map(int(n_layers), int(pattern), int(n_shared), full, tgt),
+           "psw_kv_share_map")
+    return [bool(x) for x in full], [int(x) for x in tgt]
 
 
 def get_error(stream=None) -> int:

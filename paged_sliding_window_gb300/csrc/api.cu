@@ -345,6 +345,70 @@ int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t*
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+int qkv_norm_rope_cache_write(const psw_layer_t* layer, const psw_norm_rope_t* rn,
+                              const void* q, const void* k, const void* v,
+                              const int32_t* cu_new, const int32_t* past_lens, int32_t n_seqs,
+                              const psw_pages_t* pages, void* q_out, void* k_pool, void* v_pool,
+                              psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (rn == nullptr || q == nullptr || q_out == nullptr || cu_new == nullptr ||
+      past_lens == nullptr)
+    return PSW_ENULL;
+  if (!(rn->theta > 0.f) || !isfinite(rn->theta) || !(rn->partial_rotary_factor > 0.f) ||
+      !(rn->partial_rotary_factor <= 1.f) || !(rn->eps >= 0.f) || !isfinite(rn->eps))
+    return PSW_EINVAL_ROPE;
+  const bool cache = k != nullptr;
+  if (cache) {
+    if (k_pool == nullptr) return PSW_ENULL;
+    if ((rc = check_v(L, v)) != PSW_OK) return rc;
+    if ((rc = check_v(L, v_pool)) != PSW_OK) return rc;
+    if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  } else if (v != nullptr || k_pool != nullptr || v_pool != nullptr) {
+    return PSW_ENULL;  // a q-only call names no K/V rows and no pools
+  }
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (!aligned16(q) || !aligned16(q_out) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(rn->q_weight) ||
+      !aligned16(rn->k_weight) || !aligned16(rn->v_weight))
+    return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  NormRopeArgs R;
+  R.theta = rn->theta;
+  R.eps = rn->eps;
+  R.rope_angles = static_cast<int>(rn->partial_rotary_factor * static_cast<float>(L.hd) / 2.f);
+  if (R.rope_angles > L.hd / 2) R.rope_angles = L.hd / 2;
+  R.q_weight = rn->q_weight;
+  R.k_weight = rn->k_weight;
+  R.v_weight = rn->v_weight;
+  return launch_qkv_norm_rope(L, R, q, k, v, cu_new, past_lens, n_seqs,
+                              cache ? pages->block_table : nullptr,
+                              cache ? pages->max_blocks_per_seq : 0,
+                              cache ? pages->num_blocks : 0, q_out, k_pool, v_pool,
+                              st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int psw_kv_share_map(int32_t n_layers, int32_t pattern, int32_t n_shared, int32_t* is_full,
+                     int32_t* target) {
+  if (n_layers <= 0 || pattern <= 0 || n_shared < 0 || n_shared >= n_layers)
+    return PSW_EINVAL_LAYERS;
+  const int32_t owners = n_layers - n_shared;
+  // last cache-owning layer of each type (-1: none)
+  int32_t last_owner[2] = {-1, -1};
+  for (int32_t i = 0; i < owners; ++i) last_owner[(i + 1) % pattern == 0 ? 1 : 0] = i;
+  for (int32_t i = owners; i < n_layers; ++i)
+    if (last_owner[(i + 1) % pattern == 0 ? 1 : 0] < 0) return PSW_EINVAL_LAYERS;
+  for (int32_t i = 0; i < n_layers; ++i) {
+    const int full = (i + 1) % pattern == 0 ? 1 : 0;
+    if (is_full != nullptr) is_full[i] = full;
+    if (target != nullptr) target[i] = i < owners ? i : last_owner[full];
+  }
+  return PSW_OK;
+}
+
 int psw_get_error(psw_stream_t stream, int32_t* device_error_out) {
   if (device_error_out == nullptr) return PSW_ENULL;
   DeviceState* st = current_device();
@@ -381,6 +445,11 @@ const char* psw_strerror(int code) {
     case PSW_ETENSORMAP: return "could not build the TMA descriptor of a pool";
     case PSW_ESCRATCH:
       return "batch needs more scratch than the static buffer of attn_decode_paged_noalloc";
+    case PSW_EINVAL_LAYERS:
+      return "n_layers and pattern must be > 0, n_shared in [0, n_layers), and every shared "
+             "layer needs a cache-owning layer of its type";
+    case PSW_EINVAL_ROPE:
+      return "theta must be > 0, partial_rotary_factor in (0, 1], eps >= 0, all finite";
     default: return "unknown error";
   }
 }

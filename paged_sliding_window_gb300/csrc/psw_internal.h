@@ -72,6 +72,21 @@ int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse, void* ws,
                   size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream);
 
+// Pre-attention step parameters after validation.
+struct NormRopeArgs {
+  float theta, eps;
+  int rope_angles;  // rotated pairs: floor(partial_rotary_factor * head_dim / 2)
+  const float *q_weight, *k_weight, *v_weight;
+};
+
+// Per-head RMS-norm of q (and k, v when given), proportional RoPE of q and
+// k, q into q_out and k / v into their pages. Returns a PSW_* code.
+int launch_qkv_norm_rope(const LayerArgs& L, const NormRopeArgs& R, const void* q, const void* k,
+                         const void* v, const int32_t* cu_new, const int32_t* past_lens,
+                         int n_seqs, const int32_t* block_table, int max_blocks,
+                         int64_t num_blocks, void* q_out, void* k_pool, void* v_pool, int num_sms,
+                         int32_t* err, cudaStream_t stream);
+
 // Prefill workspace: a work list of the (sequence, block) units.
 size_t prefill_workspace_bytes(const LayerArgs& L, int n_seqs, int max_q_len);
 

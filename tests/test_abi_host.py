@@ -225,3 +225,44 @@ def test_noalloc_without_gpu_fails_loudly(lib):
     cannot run, and nothing falls back to the CPU."""
     assert _noalloc(lib, _layer(), n=0) == -13
     assert _noalloc(lib, _layer(), n=4) == -13
+
+
+def _norm_rope(lib, layer, rn=None, q=FAKE, k=FAKE, v=FAKE, cu=FAKE, past=FAKE, n=4,
+               pages=None, q_out=FAKE, kp=FAKE, vp=FAKE, use_pages=True):
+    rn = rn or binding.PswNormRope(10000.0, 1.0, 1e-6, None, None, None)
+    pages = pages or _pages()
+    return lib.qkv_norm_rope_cache_write(ctypes.byref(layer), ctypes.byref(rn), q, k, v, cu,
+                                         past, n, ctypes.byref(pages) if use_pages else None,
+                                         q_out, kp, vp, None)
+
+
+def test_norm_rope_argument_checks(lib):
+    layer = _layer()
+    for bad in (binding.PswNormRope(0.0, 1.0, 1e-6, None, None, None),
+                binding.PswNormRope(float("inf"), 1.0, 1e-6, None, None, None),
+                binding.PswNormRope(1e4, 0.0, 1e-6, None, None, None),
+                binding.PswNormRope(1e4, 1.5, 1e-6, None, None, None),
+                binding.PswNormRope(1e4, 1.0, -1.0, None, None, None),
+                binding.PswNormRope(1e4, 1.0, float("nan"), None, None, None)):
+        assert _norm_rope(lib, layer, rn=bad) == -17
+    assert _norm_rope(lib, _layer(head_dim=128)) == -3
+    assert _norm_rope(lib, layer, q=None) == -1
+    assert _norm_rope(lib, layer, q_out=None) == -1
+    assert _norm_rope(lib, layer, kp=None) == -1
+    assert _norm_rope(lib, layer, v=None) == -7          # V rows missing on a k_eq_v = 0 layer
+    keqv = _layer(k_eq_v=1, n_q_heads=32, n_kv_heads=4, head_dim=512, window=0)
+    assert _norm_rope(lib, keqv) == -7                   # V rows given on a k_eq_v layer
+    assert _norm_rope(lib, layer, k=None) == -1          # q only, but V rows named
+    assert _norm_rope(lib, layer, q=FAKE + 8) == -12
+    assert _norm_rope(lib, layer, n=-1) == -9
+    assert _norm_rope(lib, layer, pages=_pages(mbps=0)) == -11
+    w = binding.PswNormRope(1e4, 1.0, 1e-6, FAKE + 4, None, None)
+    assert _norm_rope(lib, layer, rn=w) == -12
+    assert _norm_rope(lib, layer, n=0) == 0
+    # q only (a layer reading another layer's cache): no pages needed
+    assert _norm_rope(lib, layer, k=None, v=None, kp=None, vp=None, n=0, use_pages=False) == 0
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
+def test_norm_rope_without_gpu_fails_loudly(lib):
+    assert _norm_rope(lib, _layer()) == -13

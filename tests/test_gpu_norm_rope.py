@@ -1,0 +1,174 @@
+"""The fused pre-attention step on the GPU (qkv_norm_rope_cache_write: per-head
+RMS-norm, proportional RoPE of q and k, cache write of k and v) against the
+fp64 oracle.
+
+Bar (derived in gpu_harness.assert_norm_rope_close): each bf16 result within
+half a bf16 unit of the oracle's exact fp64 value plus the kernel's fp32
+error, 2^-20 (|y_d| + |y_partner|) in the normalised values of its rotation
+pair. In practice nearly every result is the oracle's own rounding; the
+share that is not is also bounded (below 1e-3). Every pool slot that is not
+written must keep its bits."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import GpuStep, NormRopeCase, assert_close, assert_norm_rope_close, host_bits
+from paged_sliding_window_gb300 import binding
+from paged_sliding_window_gb300 import workloads as wl
+from paged_sliding_window_gb300.staging import dev_bf16
+from paged_sliding_window_gb300.workloads import Layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    return oracle.default()
+
+
+def _written_slots(step):
+    """Pool rows (block, offset) of the step's new tokens."""
+    rows = []
+    for b in range(step.n_seqs):
+        for i in range(int(step.new_lens[b])):
+            pos = int(step.past_lens[b]) + i
+            rows.append((int(step.block_table[b, pos // 16]), pos % 16))
+    return rows
+
+
+def _check_pools(g_pool, before, exact, pre, rotated, step, what):
+    """New rows within the bar of the oracle's exact rows, every other slot
+    unchanged."""
+    got = host_bits(g_pool)
+    slots = _written_slots(step)
+    idx = tuple(np.array(slots).T)
+    assert_norm_rope_close(got[idx], exact, pre, rotated, f"{what} new rows")
+    mask = np.ones(got.shape[:2], bool)
+    mask[idx] = False
+    assert np.array_equal(got[mask], before[mask]), f"{what}: a slot outside the step changed"
+
+
+def _check_q(case, got_bits, with_kv=True):
+    exact_q = case.oracle_exact(with_kv)[0]
+    pre_q = case.oracle_exact(with_kv, rotate=False)[0]
+    assert_norm_rope_close(got_bits, exact_q, pre_q, True, "q_out")
+    ref_q = case.oracle(with_kv)[0]
+    assert float((got_bits != ref_q).mean()) < 1e-3, "q_out: too many results off the oracle's rounding"
+
+
+def run_case(orc, case, check_v=True):
+    g = GpuStep(case.step)
+    k_before = host_bits(g.k_pool)
+    v_before = None if g.v_pool is None else host_bits(g.v_pool)
+    out = case.gpu(g)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    _check_q(case, host_bits(out))
+    _, ek, ev = case.oracle_exact()
+    _, pk, pv = case.oracle_exact(rotate=False)
+    _check_pools(g.k_pool, k_before, ek, pk, True, case.step, "K")
+    if check_v and g.v_pool is not None:
+        _check_pools(g.v_pool, v_before, ev, pv, False, case.step, "V")
+    return g, out
+
+
+def test_norm_rope_sliding_layer(orc):
+    """Sliding layer (head_dim 256, theta 1e4, every dim rotated, weighted q/k
+    norms, weightless v norm): decode tokens and prefill chunks, ragged."""
+    layer = Layer(16, 8, 256, window=1024)
+    past = [0, 1, 15, 16, 1000, 4095, 3000, 0, 777]
+    new = [1, 1, 1, 1, 1, 1, 200, 130, 64]
+    run_case(orc, NormRopeCase(orc, layer, past, new, 101, 1e4, 1.0))
+
+
+def test_norm_rope_full_layer_partial_k_eq_v(orc):
+    """Full layer (head_dim 512, theta 1e6, a quarter of the dims rotated), V
+    aliasing the K pages: only K is written."""
+    layer = Layer(32, 4, 512, window=0, k_eq_v=True)
+    run_case(orc, NormRopeCase(orc, layer, [0, 20000, 5, 2047], [3, 1, 100, 17], 102, 1e6, 0.25,
+                               eps=1e-5))
+
+
+def test_norm_rope_v_from_the_k_projection(orc):
+    """A layer without its own V projection that keeps a V cache: V is the
+    same raw rows as K, only normalised (with a v weight), K normalised and
+    rotated."""
+    layer = Layer(16, 2, 512, window=0)
+    run_case(orc, NormRopeCase(orc, layer, [10, 300], [40, 1], 103, 1e6, 0.5, v_from_k=True,
+                               v_weight=True))
+
+
+def test_norm_rope_large_positions(orc):
+    """Positions up to about 70000, where a float angle would be off by far
+    more than a bf16 unit."""
+    layer = Layer(4, 2, 512, window=0)
+    run_case(orc, NormRopeCase(orc, layer, [65530, 69000, 40000], [8, 1, 3], 104, 1e6, 1.0))
+
+
+def test_norm_rope_q_only_leaves_pools(orc):
+    """A layer reading another layer's cache: only q is processed, in place,
+    and no pool changes."""
+    layer = Layer(16, 8, 256, window=1024)
+    case = NormRopeCase(orc, layer, [100, 3000], [1, 33], 105, 1e4, 1.0)
+    g = GpuStep(case.step)
+    k_before, v_before = host_bits(g.k_pool), host_bits(g.v_pool)
+    q = dev_bf16(case.q_raw)
+    case.gpu(g, with_kv=False, q_out=q)  # in place
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    _check_q(case, host_bits(q), with_kv=False)
+    assert np.array_equal(host_bits(g.k_pool), k_before)
+    assert np.array_equal(host_bits(g.v_pool), v_before)
+
+
+def test_norm_rope_bad_block_is_flagged_q_still_written(orc):
+    layer = Layer(16, 8, 256, window=64)
+    case = NormRopeCase(orc, layer, [100, 20], [1, 1], 106, 1e4, 1.0)
+    g = GpuStep(case.step)
+    bad = g.table.clone()
+    bad[0, 100 // 16] = case.step.cache.num_blocks + 3
+    g.pages = binding.make_pages(bad, case.step.cache.num_blocks)
+    out = case.gpu(g)
+    assert binding.get_error() & binding.DEVERR_BLOCK_ID
+    _check_q(case, host_bits(out))
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_fused_step_then_attention_matches_oracle_pipeline(orc, mode):
+    """The layer path from raw projections: fused step, then decode or chunked
+    prefill, against the oracle doing the same (its own rounding, its own
+    cache write, its own attention). Scale 1/16 keeps the softmax away from
+    near ties, where a one-unit bf16 difference in an input could move the
+    output by more than the attention bar."""
+    layer = Layer(8, 4, 256, window=256, softcap=50.0, scale=1.0 / 16)
+    if mode == "decode":
+        past, new = [300, 17, 1000, 2], [1, 1, 1, 1]
+    else:
+        past, new = [0, 200, 900], [100, 64, 300]
+    case = NormRopeCase(orc, layer, past, new, 107, 1e4, 1.0)
+    g = GpuStep(case.step)
+    q = case.gpu(g)
+    g.q = q
+    if mode == "decode":
+        g.decode()
+    else:
+        g.prefill()
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    # oracle pipeline: history, then the step's own rounded rows, then attention
+    ref_q, ref_k, ref_v = case.oracle()
+    st = case.step
+    c = st.cache
+    kp, vp = c.empty_pools()
+    orc.kv_cache_write(c.hist_k, c.hist_v, c.hist_cu, c.hist_past, st.block_table, kp, vp,
+                       in_place=True)
+    orc.kv_cache_write(ref_k, ref_v, st.cu_new, st.past_lens, st.block_table, kp, vp,
+                       in_place=True)
+    L = layer.as_dict()
+    if mode == "decode":
+        ref_o, ref_l, _ = orc.decode(L, ref_q, kp, vp, st.block_table, st.seq_lens)
+    else:
+        ref_o, ref_l, _ = orc.prefill(L, ref_q, st.cu_new, st.past_lens, kp, vp, st.block_table)
+    assert_close(g.out.cpu().numpy(), ref_o, f"{mode} out after the fused step")
+    assert_close(g.lse.cpu().numpy(), ref_l, f"{mode} lse after the fused step")
