@@ -89,6 +89,8 @@ typedef struct CUstream_st *psw_stream_t;
                                      or one of them not finite */
 #define PSW_EINVAL_LAYERS    -18  /* n_layers or pattern <= 0, n_shared outside [0, n_layers),
                                      or a shared layer with no cache-owning layer of its type */
+#define PSW_ENOBLOCKS        -19  /* the block pool has fewer free blocks than asked for */
+#define PSW_EBLOCK           -20  /* a block id outside the pool, or freed more often than held */
 
 /* ---- device error bits (psw_get_error) ---- */
 #define PSW_DEVERR_BLOCK_ID    1  /* block id outside [0, num_blocks): access skipped */
@@ -312,6 +314,68 @@ PSW_API int qkv_norm_rope_cache_write(const psw_layer_t *layer, const psw_norm_r
  */
 PSW_API int psw_kv_share_map(int32_t n_layers, int32_t pattern, int32_t n_shared,
                              int32_t *is_full, int32_t *target);
+
+/*
+ * ---- host page allocator with prefix caching (no GPU involved)
+ *
+ * The abstractions of "Gemma 4 model architecture analysis" (vLLM-Kunlun),
+ * section 6.2: each physical page (block) carries {block_id, ref_cnt,
+ * block_hash}; the pool keeps unreferenced pages in a free queue in
+ * least-recently-freed order; a sequence's block-table row lists its pages
+ * (the int32 rows every attention call takes). Section 6.6, prefix caching:
+ * a full page is named by the hash of its 16 tokens chained with the previous
+ * page's hash, and a request whose prefix matches cached pages shares those
+ * physical pages (a hit raises the page's reference count; the KV of those
+ * tokens is not computed again). Freed pages keep their hash until the queue
+ * hands them out again, so a later request can still hit them.
+ * The hash is FNV-1a over 64 bits (the parent hash as 8 little-endian bytes,
+ * then each token as 4): not a cryptographic hash; two different prefixes
+ * collide with probability about n^2 / 2^65 for n cached pages.
+ * Every call takes the pool's lock. Block ids are int32 in [0, num_blocks).
+ */
+typedef struct psw_block_pool psw_block_pool_t;
+
+/* Creates a pool of num_blocks free pages (prefix caching on when
+ * enable_prefix_cache != 0). PSW_ECAPACITY for num_blocks outside
+ * [1, 2^31 - 1], PSW_ENOBLOCKS when the host allocation fails. */
+PSW_API int psw_block_pool_create(int64_t num_blocks, int32_t enable_prefix_cache,
+                                  psw_block_pool_t **pool_out);
+PSW_API void psw_block_pool_destroy(psw_block_pool_t *pool);
+/* Pages with ref_cnt 0 (in the free queue), or PSW_ENULL. */
+PSW_API int64_t psw_block_pool_num_free(psw_block_pool_t *pool);
+/* Takes n pages from the head of the free queue (least recently freed
+ * first), each with ref_cnt 1; a page that still carried a hash loses it.
+ * All or nothing: PSW_ENOBLOCKS when fewer than n are free. */
+PSW_API int psw_block_pool_allocate(psw_block_pool_t *pool, int32_t n, int32_t *ids_out);
+/* ref_cnt -= 1 for each id, in order; a page reaching 0 joins the tail of
+ * the free queue and keeps its hash. PSW_EBLOCK (nothing changed) for an id
+ * outside the pool or released more often than it is held. Freeing a
+ * sequence's row back to front puts its last pages first in line for reuse. */
+PSW_API int psw_block_pool_free(psw_block_pool_t *pool, const int32_t *ids, int32_t n);
+/* get_cached_block: the page cached under `hash` gets ref_cnt += 1 (leaving
+ * the free queue if it was there) and its id is returned; -1 on a miss. */
+PSW_API int psw_block_pool_get_cached(psw_block_pool_t *pool, uint64_t hash, int32_t *id_out);
+/* Names a referenced page by the hash of its (now written) tokens; a hash
+ * already naming another page keeps that page. PSW_EBLOCK for a page not
+ * held by anyone. */
+PSW_API int psw_block_pool_cache(psw_block_pool_t *pool, int32_t id, uint64_t hash);
+PSW_API int psw_block_pool_ref_count(psw_block_pool_t *pool, int32_t id, int32_t *ref_out);
+/* Chained page hash: FNV-1a of (parent, tokens[0..n)). The first page's
+ * parent is 0. */
+PSW_API uint64_t psw_block_hash(uint64_t parent, const int32_t *tokens, int32_t n);
+/* Admits a request of n_tokens prompt tokens: walks its full pages (all but
+ * the page holding the last token, whose query must run) through the prefix
+ * cache until the first miss, then allocates the rest. Writes the block-table
+ * row (ceil(n_tokens / 16) ids, -1 up to max_blocks) and the number of
+ * leading tokens whose KV is already in the pages (the request's past length
+ * for its first prefill chunk). On an error nothing stays held. */
+PSW_API int psw_block_pool_admit(psw_block_pool_t *pool, const int32_t *tokens,
+                                 int32_t n_tokens, int32_t *table_row, int32_t max_blocks,
+                                 int32_t *n_cached_tokens);
+/* After the request's KV is written: names each full page of the row by its
+ * chained hash so that later requests can share it. */
+PSW_API int psw_block_pool_commit(psw_block_pool_t *pool, const int32_t *tokens,
+                                  int32_t n_tokens, const int32_t *table_row);
 
 /*
  * Synchronises `stream`, then returns the current device's error word (an OR

@@ -23,12 +23,16 @@ ERRORS = {
     -8: "PSW_EINVAL_SCALE", -9: "PSW_EINVAL_NSEQS", -10: "PSW_EWORKSPACE",
     -11: "PSW_ECAPACITY", -12: "PSW_EALIGN", -13: "PSW_EDEVICE", -14: "PSW_ELAUNCH",
     -15: "PSW_ETENSORMAP", -16: "PSW_ESCRATCH", -17: "PSW_EINVAL_ROPE",
-    -18: "PSW_EINVAL_LAYERS",
+    -18: "PSW_EINVAL_LAYERS", -19: "PSW_ENOBLOCKS", -20: "PSW_EBLOCK",
 }
 DEVERR_BLOCK_ID, DEVERR_CAPACITY, DEVERR_LENGTH, DEVERR_PIPELINE = 1, 2, 4, 8
 EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
             "attn_prefill_chunked", "psw_get_error", "psw_strerror",
-            "attn_decode_paged_noalloc", "qkv_norm_rope_cache_write", "psw_kv_share_map")
+            "attn_decode_paged_noalloc", "qkv_norm_rope_cache_write", "psw_kv_share_map",
+            "psw_block_pool_create", "psw_block_pool_destroy", "psw_block_pool_num_free",
+            "psw_block_pool_allocate", "psw_block_pool_free", "psw_block_pool_get_cached",
+            "psw_block_pool_cache", "psw_block_pool_ref_count", "psw_block_hash",
+            "psw_block_pool_admit", "psw_block_pool_commit")
 
 
 class PswLayer(ctypes.Structure):
@@ -91,6 +95,26 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.psw_kv_share_map.argtypes = [i32, i32, i32, ctypes.POINTER(i32),
                                          ctypes.POINTER(i32)]
         lib.psw_kv_share_map.restype = ctypes.c_int
+        i32p, u64 = ctypes.POINTER(i32), ctypes.c_uint64
+        lib.psw_block_pool_create.argtypes = [i64, i32, ctypes.POINTER(vp)]
+        lib.psw_block_pool_destroy.argtypes = [vp]
+        lib.psw_block_pool_destroy.restype = None
+        lib.psw_block_pool_num_free.argtypes = [vp]
+        lib.psw_block_pool_num_free.restype = i64
+        lib.psw_block_pool_allocate.argtypes = [vp, i32, i32p]
+        lib.psw_block_pool_free.argtypes = [vp, i32p, i32]
+        lib.psw_block_pool_get_cached.argtypes = [vp, u64, i32p]
+        lib.psw_block_pool_cache.argtypes = [vp, i32, u64]
+        lib.psw_block_pool_ref_count.argtypes = [vp, i32, i32p]
+        lib.psw_block_hash.argtypes = [u64, i32p, i32]
+        lib.psw_block_hash.restype = u64
+        lib.psw_block_pool_admit.argtypes = [vp, i32p, i32, i32p, i32, i32p]
+        lib.psw_block_pool_commit.argtypes = [vp, i32p, i32, i32p]
+        for name in ("psw_block_pool_create", "psw_block_pool_allocate", "psw_block_pool_free",
+                     "psw_block_pool_get_cached", "psw_block_pool_cache",
+                     "psw_block_pool_ref_count", "psw_block_pool_admit",
+                     "psw_block_pool_commit"):
+            getattr(lib, name).restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.psw_strerror.argtypes = [ctypes.c_int]
         lib.psw_strerror.restype = ctypes.c_char_p
@@ -265,6 +289,78 @@ def kv_share_map(n_layers: int, pattern: int, n_shared: int = 0):
     _raise(load().psw_kv_share_map(int(n_layers), int(pattern), int(n_shared), full, tgt),
            "psw_kv_share_map")
     return [bool(x) for x in full], [int(x) for x in tgt]
+
+
+def _i32_array(values):
+    arr = (ctypes.c_int32 * max(1, len(values)))(*[int(v) for v in values])
+    return arr
+
+
+def block_hash(parent: int, tokens) -> int:
+    """psw_block_hash: chained FNV-1a hash of one page's tokens."""
+    return int(load().psw_block_hash(int(parent), _i32_array(tokens), len(tokens)))
+
+
+class BlockPool:
+    """Host page allocator with prefix caching (psw_block_pool_*): ctypes
+    marshalling only; the pool lives in libpsw."""
+
+    def __init__(self, num_blocks: int, prefix_cache: bool = True):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _raise(self._lib.psw_block_pool_create(int(num_blocks), int(bool(prefix_cache)),
+                                               ctypes.byref(h)), "psw_block_pool_create")
+        self._h = h
+
+    def close(self):
+        if self._h:
+            self._lib.psw_block_pool_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(self._lib.psw_block_pool_num_free(self._h))
+
+    def allocate(self, n: int):
+        """(status, ids)."""
+        out = (ctypes.c_int32 * max(1, n))()
+        rc = self._lib.psw_block_pool_allocate(self._h, int(n), out)
+        return rc, (list(out[:n]) if rc == PSW_OK else [])
+
+    def release(self, ids) -> int:
+        return self._lib.psw_block_pool_free(self._h, _i32_array(ids), len(ids))
+
+    def get_cached(self, h: int) -> int:
+        out = ctypes.c_int32(-1)
+        _raise(self._lib.psw_block_pool_get_cached(self._h, int(h), ctypes.byref(out)),
+               "psw_block_pool_get_cached")
+        return int(out.value)
+
+    def cache(self, block: int, h: int) -> int:
+        return self._lib.psw_block_pool_cache(self._h, int(block), int(h))
+
+    def ref_count(self, block: int) -> int:
+        out = ctypes.c_int32(0)
+        _raise(self._lib.psw_block_pool_ref_count(self._h, int(block), ctypes.byref(out)),
+               "psw_block_pool_ref_count")
+        return int(out.value)
+
+    def admit(self, tokens, max_blocks: int):
+        """(status, block-table row, tokens whose KV is already cached)."""
+        row = (ctypes.c_int32 * max(1, max_blocks))()
+        cached = ctypes.c_int32(0)
+        rc = self._lib.psw_block_pool_admit(self._h, _i32_array(tokens), len(tokens), row,
+                                            int(max_blocks), ctypes.byref(cached))
+        return rc, (list(row[:max_blocks]) if rc == PSW_OK else None), int(cached.value)
+
+    def commit(self, tokens, row) -> int:
+        return self._lib.psw_block_pool_commit(self._h, _i32_array(tokens), len(tokens),
+                                               _i32_array(row))
 
 
 def get_error(stream=None) -> int:

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpsw.so")
 SOURCES = ["api.cu", "kv_cache_write.cu", "decode.cu", "decode_noalloc.cu", "prefill.cu",
-           "norm_rope.cu"]
+           "norm_rope.cu", "block_pool.cpp"]
 HEADERS = ["ptx.cuh", "psw_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

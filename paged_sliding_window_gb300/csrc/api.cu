@@ -445,6 +445,8 @@ const char* psw_strerror(int code) {
     case PSW_ETENSORMAP: return "could not build the TMA descriptor of a pool";
     case PSW_ESCRATCH:
       return "batch needs more scratch than the static buffer of attn_decode_paged_noalloc";
+    case PSW_ENOBLOCKS: return "the block pool has fewer free blocks than asked for";
+    case PSW_EBLOCK: return "block id outside the pool, or freed more often than it is held";
     case PSW_EINVAL_LAYERS:
       return "n_layers and pattern must be > 0, n_shared in [0, n_layers), and every shared "
              "layer needs a cache-owning layer of its type";
