@@ -396,12 +396,22 @@ def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
 
 
 def flush_l2(buf):
-    buf.add_(1)
+    """Evicts the previous call's data from L2 by reading a buffer larger than
+    L2 (a read leaves clean lines, so no write-back of unrelated dirty data
+    lands inside the next timed call)."""
+    torch = sys.modules["torch"]
+    if not hasattr(flush_l2, "_sink"):
+        flush_l2._sink = torch.empty((), dtype=buf.dtype, device=buf.device)
+    torch.sum(buf, dim=0, out=flush_l2._sink)
 
 
-def time_calls(fn, n, warmup, flush=None):
+def time_calls(fn, n, warmup, flush=None, head_start_cycles=200_000):
     """Mean CUDA-event time (ms) of fn() on the current stream, L2 flushed
-    before each timed call when `flush` is given."""
+    before each timed call when `flush` is given. The GPU spins for
+    `head_start_cycles` (about 0.1 ms) between the flush and the start event,
+    so the host has enqueued fn's launches before the start event is reached
+    and the interval holds the device work only, not the host's time spent in
+    the binding."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -410,6 +420,8 @@ def time_calls(fn, n, warmup, flush=None):
     for _ in range(n):
         if flush is not None:
             flush()
+        if head_start_cycles:
+            torch.cuda._sleep(head_start_cycles)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
@@ -440,7 +452,7 @@ def measure_prefill(steps, warmup, tflops_peak, peak_kind):
             "kv_cache_write_ms": write_ms, "flops_per_call": flops,
             "config": {"n_seqs": 8, "past": "uniform [0, 8192]", "chunk": 512, "head_dim": 256,
                        "n_q_heads": 8, "n_kv_heads": 4, "window": 1024, "softcap": 50.0,
-                       "scale": 1 / 16, "l2": "flushed (256 MB write) before every timed call"},
+                       "scale": 1 / 16, "l2": "flushed (256 MB read) before every timed call"},
             "roofline": {"bound": "tensor", "kernel": "prefill_kernel<256, false>",
                          "achieved": achieved, "peak": tflops_peak, "unit": "TFLOP/s",
                          "frac": achieved / tflops_peak, "peak_kind": peak_kind + " bf16 burst",
@@ -511,7 +523,7 @@ def measure_pre_attention(steps, warmup, hbm, peak_kind):
                                   "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": None}}
         del g
     return {"workload": "fused pre-attention step (q/k/v RMS-norm, RoPE, cache write)",
-            "l2": "flushed (256 MB write) before every timed call", **res,
+            "l2": "flushed (256 MB read) before every timed call", **res,
             "gpu_launches_per_call": 1}
 
 
@@ -619,6 +631,15 @@ def ncu_case(which):
         g.write_new()
         for _ in range(3):
             g.prefill()
+    elif which == "pre_attention":
+        from paged_sliding_window_gb300 import binding
+        step = first_step("chunked_prefill")
+        g = GpuStep(step)
+        rn = binding.make_norm_rope(1e4, 1.0, 1e-6)
+        q_out = torch.empty_like(g.q)
+        for _ in range(3):
+            binding.qkv_norm_rope_cache_write(step.layer, rn, g.q, g.new_k, g.new_v, g.cu_new,
+                                              g.past, g.pages, q_out, g.k_pool, g.v_pool)
     elif which == "decode":
         full = wl.sliding_decode().steps[0]
         ss = np.random.SeedSequence(2)
@@ -697,7 +718,7 @@ def main():
                     help="skip the prefill, full-layer decode and mixed-step measurements")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
     ap.add_argument("--ncu-case", choices=["decode", "prefill", "full_decode",
-                                           "mixed_full_prefill"], default=None)
+                                           "mixed_full_prefill", "pre_attention"], default=None)
     args = ap.parse_args()
     if args.ncu_case:
         ncu_case(args.ncu_case)

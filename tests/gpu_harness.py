@@ -86,7 +86,8 @@ def bf16_values(bits) -> np.ndarray:
 
 def assert_norm_rope_close(got_bits, exact, pre, rotated: bool, what: str):
     """Bar of the fused pre-attention step, from its arithmetic: the kernel
-    forms each result in fp32, y = x / rms * w to about 2^-21 relative and
+    forms each result in fp32, y = x / rms * w to about 2^-21 relative (its
+    reciprocal square root is good to about 2^-22) and
     out = y_d cos - y_partner sin from cos and sin good to 2^-22, so before its
     single rounding to bf16 it is within 2^-20 (|y_d| + |y_partner|) of the
     exact value; the rounding adds at most half a bf16 unit of the result.
