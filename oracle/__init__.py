@@ -90,6 +90,22 @@ class Oracle:
             ctypes.c_int32, ctypes.c_int64, _f64p]
         lib.oracle_to_bf16.restype = ctypes.c_uint16
         lib.oracle_to_bf16.argtypes = [ctypes.c_double]
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_encode_array.argtypes = [_f32p, _u8p, ctypes.c_int64]
+        lib.oracle_e4m3_decode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [_u8p, _f64p, ctypes.c_int64]
+        lib.oracle_kv_cache_write_fp8.restype = ctypes.c_int32
+        lib.oracle_kv_cache_write_fp8.argtypes = [
+            _u16p, _u16p, _i32p, _i32p, ctypes.c_int32, _i32p, ctypes.c_int32,
+            ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            _u8p, _u8p, _f32p, _f32p]
+        lib.oracle_attention_rows_fp8.restype = ctypes.c_int32
+        lib.oracle_attention_rows_fp8.argtypes = [
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_double, ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
+            _u16p, _i32p, _i64p, ctypes.c_int64, _u8p, _u8p, _f32p, _f32p, _i32p,
+            ctypes.c_int32, _f64p, _f64p, ctypes.c_int32]
         lib.oracle_to_bf16_array.restype = None
         lib.oracle_to_bf16_array.argtypes = [_f64p, _u16p, ctypes.c_int64]
         lib.oracle_qkv_norm_rope.restype = None
@@ -254,6 +270,70 @@ class Oracle:
         return out
 
 
+    # ---------------------------------------------------------- FP8 pages
+    def e4m3_encode(self, x) -> np.ndarray:
+        """OCP E4M3 codes of float32 values (nearest even, saturating at 448)."""
+        a = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(a.shape, dtype=np.uint8)
+        self.lib.oracle_e4m3_encode_array(_ptr(a, ctypes.c_float), _ptr(out, ctypes.c_uint8),
+                                          a.size)
+        return out
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, dtype=np.float64)
+        self.lib.oracle_e4m3_decode_array(_ptr(c, ctypes.c_uint8), _ptr(out, ctypes.c_double),
+                                          c.size)
+        return out
+
+    def kv_cache_write_fp8(self, k_new, v_new, cu_new, past_lens, block_table, k8, v8,
+                           k_scale, v_scale, block_size: int = 16) -> int:
+        """Quantised cache write into FP8 pools (uint8 [nb, bs, n_kv, hd]) and
+        scale pools (fp32 [nb, bs, n_kv]), in place. v8 None: K only."""
+        k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+        v_new = None if v8 is None else np.ascontiguousarray(v_new, dtype=np.uint16)
+        cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
+        past_lens = np.ascontiguousarray(past_lens, dtype=np.int32)
+        block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        for a in (k8, v8, k_scale, v_scale):
+            assert a is None or a.flags["C_CONTIGUOUS"]
+        num_blocks, bs, n_kv, hd = k8.shape
+        return int(self.lib.oracle_kv_cache_write_fp8(
+            _ptr(k_new, ctypes.c_uint16), _ptr(v_new, ctypes.c_uint16),
+            _ptr(cu_new, ctypes.c_int32), _ptr(past_lens, ctypes.c_int32), past_lens.shape[0],
+            _ptr(block_table, ctypes.c_int32), block_table.shape[1], num_blocks, n_kv, hd,
+            block_size, _ptr(k8, ctypes.c_uint8), _ptr(v8, ctypes.c_uint8),
+            _ptr(k_scale, ctypes.c_float), _ptr(v_scale, ctypes.c_float)))
+
+    def decode_fp8(self, layer: dict, q, k8, v8, k_scale, v_scale, block_table, seq_lens,
+                   seqs=None, threads: int = 0):
+        """Decode attention over FP8 pages (values code * scale)."""
+        seq_lens = np.asarray(seq_lens, dtype=np.int64)
+        idx = np.arange(seq_lens.shape[0]) if seqs is None else np.asarray(seqs, dtype=np.int64)
+        q_rows = np.ascontiguousarray(np.asarray(q)[idx], dtype=np.uint16)
+        row_seq = np.ascontiguousarray(idx.astype(np.int32))
+        row_pos = np.ascontiguousarray(seq_lens[idx] - 1, dtype=np.int64)
+        block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+        n_rows = row_pos.shape[0]
+        n_q, hd = int(layer["n_q_heads"]), int(layer["head_dim"])
+        out = np.zeros((n_rows, n_q, hd), dtype=np.float64)
+        lse = np.zeros((n_rows, n_q), dtype=np.float64)
+        if n_rows == 0:
+            return out, lse, 0
+        used = self.lib.oracle_attention_rows_fp8(
+            n_q, int(layer["n_kv_heads"]), hd, int(layer["window"]), float(layer["softcap"]),
+            float(layer["scale"]), int(layer["k_eq_v"]), int(layer.get("block_size", 16)),
+            _ptr(q_rows, ctypes.c_uint16), _ptr(row_seq, ctypes.c_int32),
+            _ptr(row_pos, ctypes.c_int64), n_rows, _ptr(k8, ctypes.c_uint8),
+            _ptr(v8, ctypes.c_uint8), _ptr(k_scale, ctypes.c_float),
+            _ptr(v_scale, ctypes.c_float), _ptr(block_table, ctypes.c_int32),
+            block_table.shape[1], _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
+            int(threads))
+        if used < 0:
+            raise ValueError(f"oracle_attention_rows_fp8 failed ({used})")
+        return out, lse, int(used)
+
+
 def default() -> Oracle:
     """The oracle built from psw_oracle.c (compiled on first use)."""
     global _default
@@ -301,3 +381,11 @@ def qkv_norm_rope(*args, **kw):
 
 def to_bf16(values):
     return default().to_bf16(values)
+
+
+def kv_cache_write_fp8(*args, **kw):
+    return default().kv_cache_write_fp8(*args, **kw)
+
+
+def decode_fp8(*args, **kw):
+    return default().decode_fp8(*args, **kw)

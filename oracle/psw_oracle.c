@@ -119,6 +119,10 @@ typedef struct {
     const int64_t *row_pos;   /* [n_rows]; < 0 means an empty row */
     int64_t n_rows;
     const uint16_t *k_pool, *v_pool;
+    /* FP8 pages (fp8 != 0): e4m3 codes and one scale per (slot, KV head) */
+    int32_t fp8;
+    const uint8_t *k8, *v8;
+    const float *k_scale, *v_scale;
     const int32_t *block_table;
     int32_t max_blocks_per_seq;
     /* outputs */
@@ -128,6 +132,138 @@ typedef struct {
     int32_t n_threads;
     int32_t thread_index;
 } attn_job_t;
+
+/*
+ * ---- FP8 KV pages (e4m3 codes, one fp32 scale per slot and KV head)
+ *
+ * The pages name no KV quantisation (InfiniLM PR 581's hardening table
+ * refuses it for sliding layers); this library's format is the OCP FP8
+ * E4M3 code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448; subnormals m * 2^-9)
+ * with a per-row scale: for a row x of head_dim values with amax = max |x|,
+ *   scale = amax / 448 and code_d = e4m3(x_d * (448 / amax)),
+ * both fp32 operations rounded to nearest, the conversion rounding to
+ * nearest even and saturating at 448; an all-zero row has scale 0 and codes
+ * 0. The value a code stands for is code * scale (exact in double).
+ */
+double oracle_e4m3_decode(uint8_t c)
+{
+    int neg = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return neg ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x)
+{
+    if (x != x)
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return sign | 0x7E; /* saturate to the largest finite value */
+    int e;
+    (void)frexp(a, &e); /* a = f * 2^e, 0.5 <= f < 1: a in [2^(e-1), 2^e) */
+    int q = e - 1 - 3;  /* quantum of a normal code in that binade */
+    if (q < -9)
+        q = -9; /* subnormal quantum */
+    double n = nearbyint(ldexp(a, -q)); /* ties to even */
+    double v = ldexp(n, q);
+    if (v == 0.0)
+        return sign;
+    if (v >= 448.0)
+        return sign | 0x7E;
+    if (v < 0.015625) /* below 2^-6: subnormal code m * 2^-9 */
+        return sign | (uint8_t)n;
+    int ev;
+    double f = frexp(v, &ev); /* v = f * 2^ev, f in [0.5, 1) */
+    int mant = (int)((f * 2.0 - 1.0) * 8.0);
+    return sign | (uint8_t)(((ev - 1 + 7) << 3) | mant);
+}
+
+/* One row of the per-row quantisation (see above). */
+static void quantize_row(const uint16_t *x, int32_t n, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int32_t d = 0; d < n; ++d) {
+        uint32_t u = ((uint32_t)x[d]) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        if (fabsf(f) > amax)
+            amax = fabsf(f);
+    }
+    if (amax == 0.0f) {
+        *scale = 0.0f;
+        memset(codes, 0, (size_t)n);
+        return;
+    }
+    float inv = 448.0f / amax;
+    *scale = amax / 448.0f;
+    for (int32_t d = 0; d < n; ++d) {
+        uint32_t u = ((uint32_t)x[d]) << 16;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        codes[d] = oracle_e4m3_encode(f * inv);
+    }
+}
+
+/*
+ * reshape_and_cache into FP8 pages: as oracle_kv_cache_write, but each
+ * (token, KV head) row of head_dim values is quantised into its slot's codes
+ * (pools uint8 [num_blocks][block_size][n_kv][head_dim]) and scale (fp32
+ * [num_blocks][block_size][n_kv]). v8 / v_scale NULL: K only.
+ */
+int32_t oracle_kv_cache_write_fp8(const uint16_t *k_new, const uint16_t *v_new,
+                                  const int32_t *cu_new, const int32_t *past_lens,
+                                  int32_t n_seqs, const int32_t *block_table,
+                                  int32_t max_blocks_per_seq, int64_t num_blocks,
+                                  int32_t n_kv_heads, int32_t head_dim,
+                                  int32_t block_size, uint8_t *k8, uint8_t *v8,
+                                  float *k_scale, float *v_scale)
+{
+    int32_t status = 0;
+    for (int32_t b = 0; b < n_seqs; ++b) {
+        const int32_t *row = block_table + (int64_t)b * max_blocks_per_seq;
+        for (int32_t t = cu_new[b]; t < cu_new[b + 1]; ++t) {
+            int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]);
+            int64_t slot = oracle_slot(row, pos, block_size);
+            int64_t block_id = slot / block_size;
+            if (block_id < 0 || block_id >= num_blocks) {
+                status = -1;
+                continue;
+            }
+            for (int32_t g = 0; g < n_kv_heads; ++g) {
+                int64_t src = ((int64_t)t * n_kv_heads + g) * head_dim;
+                int64_t dst = slot * n_kv_heads + g;
+                quantize_row(k_new + src, head_dim, k8 + dst * head_dim, &k_scale[dst]);
+                if (v8 != NULL)
+                    quantize_row(v_new + src, head_dim, v8 + dst * head_dim, &v_scale[dst]);
+            }
+        }
+    }
+    return status;
+}
+
+/* Values of a K or V row (bf16 pages, or FP8 codes times their scale). */
+static void kv_row(const attn_job_t *job, const uint16_t *pool16, const uint8_t *pool8,
+                   const float *scale8, int64_t slot, int32_t g, double *out)
+{
+    const int32_t hd = job->head_dim;
+    const int64_t r = slot * job->n_kv_heads + g;
+    if (job->fp8) {
+        const double s = (double)scale8[r];
+        for (int32_t d = 0; d < hd; ++d)
+            out[d] = oracle_e4m3_decode(pool8[r * hd + d]) * s;
+    } else {
+        for (int32_t d = 0; d < hd; ++d)
+            out[d] = bf16_bits_to_double(pool16[r * hd + d]);
+    }
+}
 
 static void attend_one(const attn_job_t *job, int64_t row, int32_t h,
                        double *scores, double *acc)
@@ -140,7 +276,10 @@ static void attend_one(const attn_job_t *job, int64_t row, int32_t h,
         job->block_table + (int64_t)job->row_seq[row] * job->max_blocks_per_seq;
     const uint16_t *q = job->q_rows + (row * job->n_q_heads + h) * (int64_t)hd;
     const uint16_t *v_pool = job->k_eq_v ? job->k_pool : job->v_pool;
+    const uint8_t *v8 = job->k_eq_v ? job->k8 : job->v8;
+    const float *v_scale = job->k_eq_v ? job->k_scale : job->v_scale;
     double *out = job->out + (row * job->n_q_heads + h) * (int64_t)hd;
+    double *kv = acc + hd; /* one K or V row */
 
     for (int32_t d = 0; d < hd; ++d)
         out[d] = 0.0;
@@ -158,10 +297,10 @@ static void attend_one(const attn_job_t *job, int64_t row, int32_t h,
             continue;
         }
         int64_t slot = oracle_slot(bt_row, j, job->block_size);
-        const uint16_t *k = job->k_pool + (slot * job->n_kv_heads + g) * (int64_t)hd;
+        kv_row(job, job->k_pool, job->k8, job->k_scale, slot, g, kv);
         double dot = 0.0;
         for (int32_t d = 0; d < hd; ++d)
-            dot += bf16_bits_to_double(q[d]) * bf16_bits_to_double(k[d]);
+            dot += bf16_bits_to_double(q[d]) * kv[d];
         double s = job->scale * dot;
         if (job->softcap > 0.0)
             s = job->softcap * tanh(s / job->softcap);
@@ -180,9 +319,9 @@ static void attend_one(const attn_job_t *job, int64_t row, int32_t h,
         double w = exp(scores[j] - m);
         l += w;
         int64_t slot = oracle_slot(bt_row, j, job->block_size);
-        const uint16_t *v = v_pool + (slot * job->n_kv_heads + g) * (int64_t)hd;
+        kv_row(job, v_pool, v8, v_scale, slot, g, kv);
         for (int32_t d = 0; d < hd; ++d)
-            acc[d] += w * bf16_bits_to_double(v[d]);
+            acc[d] += w * kv[d];
     }
     for (int32_t d = 0; d < hd; ++d)
         out[d] = acc[d] / l;
@@ -197,7 +336,7 @@ static void *attn_worker(void *arg)
         if (job->row_pos[r] > max_pos)
             max_pos = job->row_pos[r];
     double *scores = (double *)malloc((size_t)(max_pos + 1) * sizeof(double));
-    double *acc = (double *)malloc((size_t)job->head_dim * sizeof(double));
+    double *acc = (double *)malloc((size_t)job->head_dim * 2 * sizeof(double));
     if (scores == NULL || acc == NULL) {
         free(scores);
         free(acc);
@@ -218,17 +357,15 @@ int32_t oracle_num_cores(void)
     return n > 0 ? (int32_t)n : 1;
 }
 
-/*
- * Attention for an arbitrary list of query rows over the paged pools.
- * Returns the number of threads used, or a negative value on bad arguments
- * or allocation failure.
- */
-int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
+/* Attention rows over bf16 pages or (fp8 != 0) FP8 pages. */
+static int32_t attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
                               int32_t head_dim, int32_t window, double softcap,
                               double scale, int32_t k_eq_v, int32_t block_size,
                               const uint16_t *q_rows, const int32_t *row_seq,
                               const int64_t *row_pos, int64_t n_rows,
                               const uint16_t *k_pool, const uint16_t *v_pool,
+                              int32_t fp8, const uint8_t *k8, const uint8_t *v8,
+                              const float *k_scale, const float *v_scale,
                               const int32_t *block_table,
                               int32_t max_blocks_per_seq, double *out,
                               double *lse, int32_t n_threads)
@@ -236,7 +373,9 @@ int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
     if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0 ||
         head_dim <= 0 || window < 0 || softcap < 0.0 || block_size <= 0)
         return -1;
-    if (!k_eq_v && v_pool == NULL)
+    if (!fp8 && !k_eq_v && v_pool == NULL)
+        return -1;
+    if (fp8 && (k8 == NULL || k_scale == NULL || (!k_eq_v && (v8 == NULL || v_scale == NULL))))
         return -1;
     if (n_threads <= 0)
         n_threads = oracle_num_cores();
@@ -267,6 +406,11 @@ int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
         j->n_rows = n_rows;
         j->k_pool = k_pool;
         j->v_pool = v_pool;
+        j->fp8 = fp8;
+        j->k8 = k8;
+        j->v8 = v8;
+        j->k_scale = k_scale;
+        j->v_scale = v_scale;
         j->block_table = block_table;
         j->max_blocks_per_seq = max_blocks_per_seq;
         j->out = out;
@@ -295,6 +439,46 @@ int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
     free(jobs);
     free(threads);
     return failed ? -2 : n_threads;
+}
+
+/*
+ * Attention for an arbitrary list of query rows over the paged pools.
+ * Returns the number of threads used, or a negative value on bad arguments
+ * or allocation failure.
+ */
+int32_t oracle_attention_rows(int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t head_dim, int32_t window, double softcap,
+                              double scale, int32_t k_eq_v, int32_t block_size,
+                              const uint16_t *q_rows, const int32_t *row_seq,
+                              const int64_t *row_pos, int64_t n_rows,
+                              const uint16_t *k_pool, const uint16_t *v_pool,
+                              const int32_t *block_table,
+                              int32_t max_blocks_per_seq, double *out,
+                              double *lse, int32_t n_threads)
+{
+    return attention_rows(n_q_heads, n_kv_heads, head_dim, window, softcap, scale,
+                          k_eq_v, block_size, q_rows, row_seq, row_pos, n_rows, k_pool,
+                          v_pool, 0, NULL, NULL, NULL, NULL, block_table,
+                          max_blocks_per_seq, out, lse, n_threads);
+}
+
+/* The same over FP8 pages: K_j = code * scale (V likewise; V reads the K
+ * codes and scales when k_eq_v). */
+int32_t oracle_attention_rows_fp8(int32_t n_q_heads, int32_t n_kv_heads,
+                                  int32_t head_dim, int32_t window, double softcap,
+                                  double scale, int32_t k_eq_v, int32_t block_size,
+                                  const uint16_t *q_rows, const int32_t *row_seq,
+                                  const int64_t *row_pos, int64_t n_rows,
+                                  const uint8_t *k8, const uint8_t *v8,
+                                  const float *k_scale, const float *v_scale,
+                                  const int32_t *block_table,
+                                  int32_t max_blocks_per_seq, double *out,
+                                  double *lse, int32_t n_threads)
+{
+    return attention_rows(n_q_heads, n_kv_heads, head_dim, window, softcap, scale,
+                          k_eq_v, block_size, q_rows, row_seq, row_pos, n_rows, NULL, NULL,
+                          1, k8, v8, k_scale, v_scale, block_table, max_blocks_per_seq,
+                          out, lse, n_threads);
 }
 
 /*
@@ -412,4 +596,17 @@ void oracle_to_bf16_array(const double *v, uint16_t *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_to_bf16(v[i]);
+}
+
+/* oracle_e4m3_encode / oracle_e4m3_decode over arrays. */
+void oracle_e4m3_encode_array(const float *x, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t *c, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_decode(c[i]);
 }

@@ -24,6 +24,7 @@ import os
 
 import numpy as np
 
+from oracle_pins_fp8 import FP8_CHECKS
 from oracle_pins_rope import ROPE_CHECKS
 from paged_sliding_window_gb300 import workloads as wl
 
@@ -461,4 +462,4 @@ ALL_CHECKS = [
     check_gqa_grouping, check_empty_sequence, check_paged_equals_contiguous,
     check_decode_equals_last_prefill_row, check_prefill_equals_sequential_decodes,
     check_softcap_to_identity, check_k_eq_v_equals_copy,
-] + ROPE_CHECKS
+] + ROPE_CHECKS + FP8_CHECKS

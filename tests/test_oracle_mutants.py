@@ -44,6 +44,13 @@ MUTANTS = [
      "int64_t pos = (int64_t)past_lens[b] + (t - cu_new[b]) + 1;\n            for (int32_t h"),
     ("bf16 rounding truncates", "double n = nearbyint(ldexp(a, -qexp));",
      "double n = floor(ldexp(a, -qexp));"),
+    ("e4m3 exponent bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3 rounds ties away", "double n = nearbyint(ldexp(a, -q)); /* ties to even */",
+     "double n = round(ldexp(a, -q));"),
+    ("fp8 scale off the code range", "*scale = amax / 448.0f;", "*scale = amax / 240.0f;"),
+    ("fp8 scale ignored", "const double s = (double)scale8[r];", "const double s = 1.0;"),
+    ("fp8 v read from k codes", "const uint8_t *v8 = job->k_eq_v ? job->k8 : job->v8;",
+     "const uint8_t *v8 = job->k8;"),
 ]
 
 
