@@ -491,6 +491,53 @@ def measure_full_decode(steps, warmup, hbm, peak_kind):
             "gpu_launches_per_call": 1}
 
 
+def fp8_kv_bytes(step: wl.Step) -> int:
+    """Algorithmic bytes of a decode launch over FP8 pages: one code byte per
+    element and one fp32 scale per (slot, KV head), for K and (unless k_eq_v)
+    V, for every visible key."""
+    L = step.layer
+    lens = step.seq_lens.astype(np.int64)
+    keys = np.minimum(lens, L.window) if L.window > 0 else lens
+    per_key = L.n_kv_heads * (L.head_dim + 4) * (1 if L.k_eq_v else 2)
+    return int(keys.sum()) * per_key
+
+
+def measure_fp8_decode(steps, warmup, hbm, peak_kind):
+    """Decode over FP8 pages (attn_decode_paged_fp8) on the sliding decode
+    batch and the full-layer k_eq_v decode: bytes moved per second, and the
+    call time against the same workload on bf16 pages (keys per second)."""
+    import torch
+    from paged_sliding_window_gb300 import binding
+    from paged_sliding_window_gb300.staging import GpuStep, GpuStepFP8
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    res = {}
+    for name, kernel in (("sliding_decode", "decode_split_kernel<256, false, true>"),
+                         ("full_keqv_decode", "decode_split_kernel<512, true, true>")):
+        step = first_step(name)
+        g8 = GpuStepFP8(step)
+        g8.write_new()
+        ms8 = time_calls(g8.decode, steps, warmup, lambda: flush_l2(scratch))
+        assert binding.get_error() == 0
+        del g8
+        g = GpuStep(step)
+        g.write_new()
+        ms16 = time_calls(g.decode, steps, warmup, lambda: flush_l2(scratch))
+        assert binding.get_error() == 0
+        del g
+        nbytes = fp8_kv_bytes(step)
+        achieved = (nbytes + io_bytes(step)) / (ms8 / 1e3) / 1e9
+        res[name] = {"ms_per_call": ms8, "bf16_pages_ms_per_call": ms16,
+                     "speedup_vs_bf16_pages": ms16 / ms8, "kv_bytes_per_call": nbytes,
+                     "value": nbytes / (ms8 / 1e3) / 1e9, "unit": "GB/s",
+                     "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved,
+                                  "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                                  "peak_kind": peak_kind, "traffic": None}}
+    return {"workload": "decode over FP8 (E4M3 + per-row fp32 scale) pages",
+            "metric": "decode attn KV-read GB/s (FP8 codes + scales)",
+            "l2": "flushed (256 MB read) before every timed call", **res,
+            "gpu_launches_per_call": 1}
+
+
 def measure_pre_attention(steps, warmup, hbm, peak_kind):
     """The fused pre-attention step (per-head RMS-norm, proportional RoPE,
     cache write) over the chunked-prefill workload's 4096 new tokens and over
@@ -640,6 +687,13 @@ def ncu_case(which):
         for _ in range(3):
             binding.qkv_norm_rope_cache_write(step.layer, rn, g.q, g.new_k, g.new_v, g.cu_new,
                                               g.past, g.pages, q_out, g.k_pool, g.v_pool)
+    elif which == "fp8_decode":
+        from paged_sliding_window_gb300.staging import GpuStepFP8
+        step = first_step("sliding_decode")
+        g = GpuStepFP8(step)
+        g.write_new()
+        for _ in range(3):
+            g.decode()
     elif which == "decode":
         full = wl.sliding_decode().steps[0]
         ss = np.random.SeedSequence(2)
@@ -718,7 +772,8 @@ def main():
                     help="skip the prefill, full-layer decode and mixed-step measurements")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-step measurement")
     ap.add_argument("--ncu-case", choices=["decode", "prefill", "full_decode",
-                                           "mixed_full_prefill", "pre_attention"], default=None)
+                                           "mixed_full_prefill", "pre_attention", "fp8_decode"],
+                    default=None)
     args = ap.parse_args()
     if args.ncu_case:
         ncu_case(args.ncu_case)
@@ -848,6 +903,7 @@ def main():
         hbm_p, tf_p, kind_p, _ = peaks()
         line["prefill"] = measure_prefill(args.steps, args.warmup, tf_p, kind_p)
         line["full_keqv_decode"] = measure_full_decode(args.steps, args.warmup, hbm_p, kind_p)
+        line["fp8_decode"] = measure_fp8_decode(args.steps, args.warmup, hbm_p, kind_p)
         line["pre_attention_step"] = measure_pre_attention(args.steps, args.warmup, hbm_p,
                                                            kind_p)
         if not args.no_mixed:

@@ -298,6 +298,43 @@ PSW_API int qkv_norm_rope_cache_write(const psw_layer_t *layer, const psw_norm_r
                                       void *k_pool, void *v_pool, psw_stream_t stream);
 
 /*
+ * ---- FP8 KV pages (e4m3), halving the bytes decode reads
+ *
+ * The pages name no KV quantisation (InfiniLM PR 581's hardening table
+ * refuses it for sliding layers); this is the library's own format. A pool
+ * holds one-byte OCP E4M3 codes in the bf16 pool's layout,
+ * uint8 [num_blocks][16][n_kv_heads][head_dim], with a scale pool fp32
+ * [num_blocks][16][n_kv_heads]: one scale per (slot, KV head) row, so the
+ * tokens of a page can be written one at a time. For a row x:
+ *   scale = amax / 448, code_d = e4m3(x_d * (448 / amax)), amax = max |x|
+ * (fp32 division and product rounded to nearest; the conversion rounds to
+ * nearest even and saturates at 448; an all-zero row has scale 0). The row
+ * stands for code_d * scale; attention runs on those values exactly (codes
+ * convert to bf16 without loss, the K scale multiplies the score, the V
+ * scale multiplies P).
+ */
+
+/* kv_cache_write into FP8 pools: arguments as kv_cache_write, with
+ * k_pool8 / v_pool8 the code pools and k_scale / v_scale (device fp32,
+ * 4-byte aligned) the scale pools; with k_eq_v, v, v_pool8 and v_scale are
+ * NULL. Errors as kv_cache_write. */
+PSW_API int kv_cache_write_fp8(const psw_layer_t *layer, const void *k, const void *v,
+                               const int32_t *cu_new, const int32_t *past_lens,
+                               int32_t n_seqs, const psw_pages_t *pages, void *k_pool8,
+                               void *v_pool8, float *k_scale, float *v_scale,
+                               psw_stream_t stream);
+
+/* attn_decode_paged over FP8 pools (arguments, results, workspace and errors
+ * as attn_decode_paged; v_pool8 and v_scale NULL with k_eq_v). The same
+ * split-KV kernel streams e4m3 tiles (half the bytes) and converts them to
+ * bf16 in shared memory before its matrix products. */
+PSW_API int attn_decode_paged_fp8(const psw_layer_t *layer, const void *q, const void *k_pool8,
+                                  const void *v_pool8, const float *k_scale,
+                                  const float *v_scale, const psw_pages_t *pages,
+                                  const int32_t *seq_lens, int32_t n_seqs, float *out,
+                                  float *lse, void *ws, size_t ws_bytes, psw_stream_t stream);
+
+/*
  * Layer types of a hybrid stack and its KV-sharing map. Host arithmetic only
  * (no GPU, nothing launched).
  *   is_full[i] = 1 when (i + 1) % pattern == 0, else 0 (sliding): the

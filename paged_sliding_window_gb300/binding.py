@@ -32,7 +32,8 @@ EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
             "psw_block_pool_create", "psw_block_pool_destroy", "psw_block_pool_num_free",
             "psw_block_pool_allocate", "psw_block_pool_free", "psw_block_pool_get_cached",
             "psw_block_pool_cache", "psw_block_pool_ref_count", "psw_block_hash",
-            "psw_block_pool_admit", "psw_block_pool_commit")
+            "psw_block_pool_admit", "psw_block_pool_commit", "kv_cache_write_fp8",
+            "attn_decode_paged_fp8")
 
 
 class PswLayer(ctypes.Structure):
@@ -115,6 +116,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                      "psw_block_pool_ref_count", "psw_block_pool_admit",
                      "psw_block_pool_commit"):
             getattr(lib, name).restype = ctypes.c_int
+        lib.kv_cache_write_fp8.argtypes = [lp, vp, vp, vp, vp, i32, pp, vp, vp, vp, vp, vp]
+        lib.kv_cache_write_fp8.restype = ctypes.c_int
+        lib.attn_decode_paged_fp8.argtypes = [lp, vp, vp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz,
+                                              vp]
+        lib.attn_decode_paged_fp8.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.psw_strerror.argtypes = [ctypes.c_int]
         lib.psw_strerror.restype = ctypes.c_char_p
@@ -249,6 +255,44 @@ def attn_decode_paged_noalloc(layer, q, k_pool, v_pool, pages: PswPages, seq_len
                                           _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(out),
                                           _ptr(lse), _stream(stream))
     _raise(rc, "attn_decode_paged_noalloc")
+
+
+def kv_cache_write_fp8(layer, k, v, cu_new, past_lens, pages: PswPages, k_pool8, v_pool8,
+                       k_scale, v_scale, stream=None) -> None:
+    """kv_cache_write into FP8 pools (uint8 codes, fp32 per-row scales)."""
+    _check(k, torch.bfloat16, "k")
+    _check(v, torch.bfloat16, "v")
+    _check(k_pool8, torch.uint8, "k_pool8")
+    _check(v_pool8, torch.uint8, "v_pool8")
+    _check(k_scale, torch.float32, "k_scale")
+    _check(v_scale, torch.float32, "v_scale")
+    _check(cu_new, torch.int32, "cu_new")
+    _check(past_lens, torch.int32, "past_lens")
+    rc = load().kv_cache_write_fp8(ctypes.byref(make_layer(layer)), _ptr(k), _ptr(v),
+                                   _ptr(cu_new), _ptr(past_lens), int(past_lens.shape[0]),
+                                   ctypes.byref(pages), _ptr(k_pool8), _ptr(v_pool8),
+                                   _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _raise(rc, "kv_cache_write_fp8")
+
+
+def attn_decode_paged_fp8(layer, q, k_pool8, v_pool8, k_scale, v_scale, pages: PswPages,
+                          seq_lens, out, lse=None, ws=None, stream=None) -> None:
+    """attn_decode_paged over FP8 pools."""
+    _check(q, torch.bfloat16, "q")
+    _check(k_pool8, torch.uint8, "k_pool8")
+    _check(v_pool8, torch.uint8, "v_pool8")
+    _check(k_scale, torch.float32, "k_scale")
+    _check(v_scale, torch.float32, "v_scale")
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(out, torch.float32, "out")
+    _check(lse, torch.float32, "lse")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().attn_decode_paged_fp8(ctypes.byref(make_layer(layer)), _ptr(q), _ptr(k_pool8),
+                                      _ptr(v_pool8), _ptr(k_scale), _ptr(v_scale),
+                                      ctypes.byref(pages), _ptr(seq_lens),
+                                      int(seq_lens.shape[0]), _ptr(out), _ptr(lse), _ptr(ws),
+                                      ws_bytes, _stream(stream))
+    _raise(rc, "attn_decode_paged_fp8")
 
 
 def make_norm_rope(theta: float, partial_rotary_factor: float = 1.0, eps: float = 1e-6,

@@ -206,6 +206,25 @@ int make_pool_page_map(CUtensorMap* map, const void* pool, int64_t num_blocks, i
   return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
 }
 
+int make_pool_tensor_map_fp8(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
+                             int hd) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return PSW_ETENSORMAP;
+  // [slot][chunk of 64 codes across (kv head, head_dim)][64 codes]; a box is
+  // 16 slots x 1 chunk = 1 KB, unswizzled (the consumers convert it with
+  // plain loads)
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(n_kv) * (hd / 64),
+                              static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  const cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(n_kv) * hd};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockSize)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  memset(map, 0, sizeof(*map));
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PSW_OK : PSW_ETENSORMAP;
+}
+
 int make_query_tensor_map(CUtensorMap* map, const void* q, int n_q_total, int n_q, int hd,
                           int group) {
   EncodeTiledFn enc = encode_fn();
@@ -292,6 +311,70 @@ int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_poo
   return launch_decode(L, q, k_map, v_map, pages->block_table, pages->max_blocks_per_seq,
                        pages->num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
                        st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+}  // namespace
+
+int kv_cache_write_fp8(const psw_layer_t* layer, const void* k, const void* v,
+                       const int32_t* cu_new, const int32_t* past_lens, int32_t n_seqs,
+                       const psw_pages_t* pages, void* k_pool8, void* v_pool8, float* k_scale,
+                       float* v_scale, psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_layer(layer, &L);
+  if (rc != PSW_OK) return rc;
+  if (k == nullptr || cu_new == nullptr || past_lens == nullptr || k_pool8 == nullptr ||
+      k_scale == nullptr)
+    return PSW_ENULL;
+  if ((rc = check_v(L, v)) != PSW_OK) return rc;
+  if ((rc = check_v(L, v_pool8)) != PSW_OK) return rc;
+  if ((rc = check_v(L, v_scale)) != PSW_OK) return rc;
+  if ((rc = check_pages(pages)) != PSW_OK) return rc;
+  if (n_seqs < 0) return PSW_EINVAL_NSEQS;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool8) || !aligned16(v_pool8) ||
+      !aligned4(k_scale) || !aligned4(v_scale))
+    return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  cudaError_t e = launch_kv_cache_write_fp8(
+      L, k, v, cu_new, past_lens, n_seqs, pages->block_table, pages->max_blocks_per_seq,
+      pages->num_blocks, k_pool8, v_pool8, k_scale, v_scale, st->info.num_sms, st->err,
+      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
+}
+
+int attn_decode_paged_fp8(const psw_layer_t* layer, const void* q, const void* k_pool8,
+                          const void* v_pool8, const float* k_scale, const float* v_scale,
+                          const psw_pages_t* pages, const int32_t* seq_lens, int32_t n_seqs,
+                          float* out, float* lse, void* ws, size_t ws_bytes,
+                          psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_decode_args(layer, q, k_pool8, v_pool8, pages, seq_lens, n_seqs, out, &L);
+  if (rc != PSW_OK) return rc;
+  if (k_scale == nullptr) return PSW_ENULL;
+  if ((rc = check_v(L, v_scale)) != PSW_OK) return rc;
+  if (!aligned4(k_scale) || !aligned4(v_scale)) return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  if (ws == nullptr) return PSW_EWORKSPACE;
+  if (ws_bytes < decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total) return PSW_EWORKSPACE;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  CUtensorMap k_map, v_map;
+  if ((rc = make_pool_tensor_map_fp8(&k_map, k_pool8, pages->num_blocks, L.n_kv, L.hd)) !=
+      PSW_OK)
+    return rc;
+  if (L.k_eq_v) {
+    v_map = k_map;
+  } else if ((rc = make_pool_tensor_map_fp8(&v_map, v_pool8, pages->num_blocks, L.n_kv,
+                                            L.hd)) != PSW_OK) {
+    return rc;
+  }
+  return launch_decode(L, q, k_map, v_map, pages->block_table, pages->max_blocks_per_seq,
+                       pages->num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
+                       st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream),
+                       k_scale, L.k_eq_v ? k_scale : v_scale);
 }
 
 int attn_prefill_chunked(const psw_layer_t* layer, const void* q, const int32_t* cu_q,

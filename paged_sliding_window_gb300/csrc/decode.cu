@@ -37,6 +37,8 @@
 //  * Rows of a partially visible page (before the window start or past the
 //    end) are masked in the scores and their V rows zeroed in shared memory,
 //    so stale or non-finite cache contents never reach the output.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "psw_internal.h"
@@ -58,7 +60,11 @@ constexpr int kCtasPerSm = 2;
 constexpr int kStageTarget = 32768;
 constexpr int kInfoInts = 16;  // shared ints: warp sums, slice start, flags
 
-template <int HD, bool KEQV>
+// FP8 pages: the ring holds e4m3 tiles (half the bytes of a bf16 tile of the
+// same keys) and their per-row scales; every consumer warp converts its own
+// quarter of head_dim of a tile into a bf16 tile of the usual layout, which
+// the unchanged QK / PV code then reads.
+template <int HD, bool KEQV, bool FP8 = false>
 struct Cfg {
   static constexpr int kChunks = HD / 64;
   static constexpr int kPageBytes = kChunks * kChunkBytes;
@@ -66,20 +72,54 @@ struct Cfg {
   static constexpr int kTileKeys = kTilePages * kBlockSize;
   static constexpr int kSRow = kTileKeys < 32 ? 32 : kTileKeys;  // score-exchange row stride
   static constexpr int kKTileBytes = kTilePages * kPageBytes;
-  static constexpr int kStageBytes = kKTileBytes * (KEQV ? 1 : 2);
-  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = kKTileBytes * (KEQV ? 1 : 2);  // one bf16 tile
+  static constexpr int kSRowF = kTileKeys < 32 ? 32 : kTileKeys;
+  // FP8 tiles are half the size: four ring stages where two CTAs per SM still fit
+  static constexpr int kStages =
+      !FP8 ? 3
+           : (1024 + 4 * (kStageBytes / 2) + kStageBytes + 4 * kTileKeys * 2 * 4 +
+                  2 * kConsumerWarps * kQHeadsPerUnit * kSRowF * 4 + 64 + 64) *
+                         kCtasPerSm <= 232448
+                 ? 4
+                 : 3;
+  // e4m3 geometry: a TMA box is 16 rows x 64 one-byte codes
+  static constexpr int kChunkBytes8 = kBlockSize * 64;
+  static constexpr int kPageBytes8 = kChunks * kChunkBytes8;
+  static constexpr int kKTileBytes8 = kTilePages * kPageBytes8;
+  static constexpr int kRingStageBytes = FP8 ? kStageBytes / 2 : kStageBytes;
+  static constexpr int kScaleFloats = kTileKeys * (KEQV ? 1 : 2);  // per ring stage
+  static constexpr int kScaleBytes = FP8 ? kStages * kScaleFloats * 4 : 0;
+  static constexpr int kConvBytes = FP8 ? kStageBytes : 0;
   static constexpr int kDPerWarp = HD / kConsumerWarps;
   static constexpr int kKSteps = kDPerWarp / 16;
   static constexpr int kMTiles = kDPerWarp / 16;
   static constexpr int kChunksPerWarp = kDPerWarp / 64;
   static constexpr int kSBufFloats = kConsumerWarps * kQHeadsPerUnit * kSRow;
   static constexpr int kTmaPerTile = kTilePages * kChunks * (KEQV ? 1 : 2);
-  static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + 2 * kSBufFloats * 4 + 2 * kStages * 8 + kInfoInts * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kRingStageBytes + kConvBytes + kScaleBytes +
+                                    2 * kSBufFloats * 4 + 2 * kStages * 8 + kInfoInts * 4;
   static_assert(kTilePages >= 1, "tile of at least one page");
   static_assert(kTmaPerTile <= 32, "one TMA box per producer lane");
   static_assert(kSmemBytes * kCtasPerSm <= 232448, "shared memory per SM");
 };
+
+// Eight e4m3 codes (8 bytes) as eight bf16 values (16 bytes). Every e4m3
+// value has at most four significant bits and an exponent in [-9, 8], so it
+// is exact in f16 and then in bf16 (the upper half of its float).
+__device__ __forceinline__ uint4 e4m3x8_to_bf16x8(uint2 in) {
+  uint32_t out[4];
+  const uint32_t w[2] = {in.x, in.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_fp8x2_storage_t pair =
+        static_cast<__nv_fp8x2_storage_t>((w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+    const float lo = __half2float(__half(__half_raw{h.x}));
+    const float hi = __half2float(__half(__half_raw{h.y}));
+    out[i] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
 
 // XOR swizzle of the key index in the score-exchange buffer: conflict-free
 // for both the fragment-layout writes and the row-wise float2 reads.
@@ -181,7 +221,7 @@ __device__ void merge_unit(int u, int c0, int c1, int nh, float* out_rows, float
 }
 
 // ---------------------------------------------------------------- split
-template <int HD, bool KEQV>
+template <int HD, bool KEQV, bool FP8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map,
@@ -190,14 +230,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     int n_seqs, int n_q, int n_kv, int group, int qchunks, int window,
                     float scale, float softcap, float* __restrict__ out,
                     float* __restrict__ lse, float* __restrict__ ws_o,
-                    float2* __restrict__ ws_ml, int32_t* __restrict__ tickets, int32_t* err) {
-  using C = Cfg<HD, KEQV>;
+                    float2* __restrict__ ws_ml, int32_t* __restrict__ tickets,
+                    const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+                    int32_t* err) {
+  using C = Cfg<HD, KEQV, FP8>;
   constexpr int TP = C::kTilePages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* stages = smem;
-  float* sbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* stages = smem;                                        // the ring
+  uint8_t* conv = stages + C::kStages * C::kRingStageBytes;      // FP8: converted tile
+  float* scales = reinterpret_cast<float*>(conv + C::kConvBytes);  // FP8: [stage][K/V][key]
+  float* sbuf = scales + C::kScaleBytes / 4;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(sbuf + 2 * C::kSBufFloats);
   uint64_t* empty_bar = full_bar + C::kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty_bar + C::kStages);
@@ -208,7 +252,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
+      // FP8: the TMA bytes plus one arrival per producer lane for the scales
+      mbar_init(&full_bar[i], FP8 ? 1 + 32 : 1);
       mbar_init(&empty_bar[i], kConsumerWarps);
     }
     *abort_flag = 0;
@@ -321,15 +366,42 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
         break;
       }
       if (lane == 0)
-        mbar_arrive_expect_tx(&full_bar[stage],
-                              static_cast<uint32_t>(npages * C::kPageBytes * (KEQV ? 1 : 2)));
+        mbar_arrive_expect_tx(
+            &full_bar[stage],
+            static_cast<uint32_t>(npages * (FP8 ? C::kPageBytes8 : C::kPageBytes) *
+                                  (KEQV ? 1 : 2)));
       __syncwarp();
       if (lane < C::kTmaPerTile && lp < npages) {
-        uint8_t* dst = stages + stage * C::kStageBytes + which * C::kKTileBytes +
-                       lp * C::kPageBytes + lc * kChunkBytes;
+        uint8_t* dst =
+            FP8 ? stages + stage * C::kRingStageBytes + which * C::kKTileBytes8 +
+                      lp * C::kPageBytes8 + lc * C::kChunkBytes8
+                : stages + stage * C::kStageBytes + which * C::kKTileBytes + lp * C::kPageBytes +
+                      lc * kChunkBytes;
         const CUtensorMap* map = (which == 0) ? &k_map : &v_map;
         tma_load_3d_hint(dst, map, &full_bar[stage], 0, kvh * C::kChunks + lc,
                          my_blk * kBlockSize, policy);
+      }
+      if constexpr (FP8) {
+        // the tile's row scales: key i of the tile from page i / 16, row i % 16
+        // (0 for pages past the sequence end or with a bad block id)
+        float* sc = scales + stage * C::kScaleFloats;
+#pragma unroll
+        for (int i0 = 0; i0 < C::kTileKeys; i0 += 32) {
+          const int i = i0 + lane;
+          const int pblk = __shfl_sync(0xffffffffu, blk, (i / kBlockSize) % 32);
+          float ks = 0.f, vs = 0.f;
+          if (i < C::kTileKeys && i / kBlockSize < npages && pblk >= 0) {
+            const int64_t r =
+                (static_cast<int64_t>(pblk) * kBlockSize + i % kBlockSize) * n_kv + kvh;
+            ks = k_scale[r];
+            if (!KEQV) vs = v_scale[r];
+          }
+          if (i < C::kTileKeys) {
+            sc[i] = ks;
+            if (!KEQV) sc[C::kTileKeys + i] = vs;
+          }
+        }
+        mbar_arrive(&full_bar[stage]);  // every lane: its scale stores are released
       }
       w.advance();
     }
@@ -416,7 +488,47 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       flag_error(err, PSW_DEVERR_PIPELINE);
       *cons_abort = 1;
     }
-    const uint32_t kbase = stages_u32 + stage * C::kStageBytes;
+    // FP8: this warp converts its quarter of head_dim of the tile (K, and V
+    // unless k_eq_v) into the bf16 tile, keeps the scales of its keys (same
+    // order as the scores below) and releases the ring stage at once
+    float ksc[TP][4], vsc[TP][4];
+    if constexpr (FP8) {
+      if (landed) {
+        const uint8_t* ring = stages + stage * C::kRingStageBytes;
+#pragma unroll
+        for (int which = 0; which < (KEQV ? 1 : 2); ++which) {
+#pragma unroll
+          for (int pg = 0; pg < TP; ++pg) {
+#pragma unroll
+            for (int cw = 0; cw < C::kChunksPerWarp; ++cw) {
+              const int c = warp * C::kChunksPerWarp + cw;
+              const uint8_t* src =
+                  ring + which * C::kKTileBytes8 + pg * C::kPageBytes8 + c * C::kChunkBytes8;
+              uint8_t* dst = conv + which * C::kKTileBytes + pg * C::kPageBytes + c * kChunkBytes;
+#pragma unroll
+              for (int idx = lane; idx < kBlockSize * 8; idx += 32) {
+                const int row = idx >> 3, u = idx & 7;  // 8 codes -> one 16-byte bf16 unit
+                const uint2 in = *reinterpret_cast<const uint2*>(src + row * 64 + u * 8);
+                *reinterpret_cast<uint4*>(dst + row * 128 + ((u ^ (row & 7)) << 4)) =
+                    e4m3x8_to_bf16x8(in);
+              }
+            }
+          }
+        }
+        const float* sc = scales + stage * C::kScaleFloats;
+#pragma unroll
+        for (int kk = 0; kk < TP; ++kk)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = kk * 16 + (e >> 1) * 8 + 2 * t4 + (e & 1);
+            ksc[kk][e] = sc[key];
+            vsc[kk][e] = KEQV ? ksc[kk][e] : sc[C::kTileKeys + key];
+          }
+        __syncwarp();  // the warp's ldmatrix reads what its lanes converted
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      }
+    }
+    const uint32_t kbase = FP8 ? smem_u32(conv) : stages_u32 + stage * C::kStageBytes;
     const uint32_t vbase = KEQV ? kbase : kbase + C::kKTileBytes;
 
     // ---- QK over this warp's quarter of head_dim: S^T[key, qh]
@@ -473,6 +585,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
           acc.y += v2.y;
         }
         float x0 = acc.x, x1 = acc.y;
+        if constexpr (FP8) {  // the key's row scale
+          x0 *= ksc[kk][2 * e];
+          x1 *= ksc[kk][2 * e + 1];
+        }
         if (use_cap) {
           x0 = softcap * tanhf(x0 * scale / softcap) * kLog2e;
           x1 = softcap * tanhf(x1 * scale / softcap) * kLog2e;
@@ -498,9 +614,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     float psum = 0.f;
     #pragma unroll
     for (int kk = 0; kk < TP; ++kk) {
-      const float p0 = exp2f(sv[kk][0] - m_new), p1 = exp2f(sv[kk][1] - m_new);
-      const float p2 = exp2f(sv[kk][2] - m_new), p3 = exp2f(sv[kk][3] - m_new);
+      float p0 = exp2f(sv[kk][0] - m_new), p1 = exp2f(sv[kk][1] - m_new);
+      float p2 = exp2f(sv[kk][2] - m_new), p3 = exp2f(sv[kk][3] - m_new);
       psum += (p0 + p1) + (p2 + p3);
+      if constexpr (FP8) {  // the V row scale folded into P (masked keys stay 0)
+        p0 = p0 > 0.f ? p0 * vsc[kk][0] : 0.f;
+        p1 = p1 > 0.f ? p1 * vsc[kk][1] : 0.f;
+        p2 = p2 > 0.f ? p2 * vsc[kk][2] : 0.f;
+        p3 = p3 > 0.f ? p3 * vsc[kk][3] : 0.f;
+      }
       pf[kk][0] = pack_bf16x2(p0, p1);
       pf[kk][1] = pack_bf16x2(p2, p3);
       const float2 h0 = unpack_bf16x2(pf[kk][0]), h1 = unpack_bf16x2(pf[kk][1]);
@@ -517,8 +639,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       const int r_lo = max(0, w.lo - pf_pos);
       const int r_hi = min(kBlockSize, w.len - pf_pos);
       if (kk < npages && (r_lo > 0 || r_hi < kBlockSize)) {
-        uint8_t* vpage = stages + stage * C::kStageBytes + (KEQV ? 0 : C::kKTileBytes) +
-                         kk * C::kPageBytes;
+        uint8_t* vpage = (FP8 ? conv : stages + stage * C::kStageBytes) +
+                         (KEQV ? 0 : C::kKTileBytes) + kk * C::kPageBytes;
         for (int idx = lane; idx < kBlockSize * 8 * C::kChunksPerWarp; idx += 32) {
           const int row = idx / (8 * C::kChunksPerWarp);
           const int rem = idx - row * (8 * C::kChunksPerWarp);
@@ -561,7 +683,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[stage]);
+    if (!FP8 && lane == 0) mbar_arrive(&empty_bar[stage]);
 
     // ---- end of this CTA's share of the unit: write the result or a partial
     const bool unit_end = (w.tile == w.ntu - 1) || (t == t_end - 1);
@@ -629,12 +751,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
   }
 }
 
-template <int HD, bool KEQV>
+template <int HD, bool KEQV, bool FP8>
 int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CUtensorMap& v_map,
            const int32_t* block_table, int max_blocks, int64_t num_blocks, const int32_t* seq_lens,
            int n_seqs, float* out, float* lse, void* ws, size_t ws_bytes, int num_sms,
-           int32_t* err, cudaStream_t stream) {
-  using C = Cfg<HD, KEQV>;
+           int32_t* err, cudaStream_t stream, const float* k_scale, const float* v_scale) {
+  using C = Cfg<HD, KEQV, FP8>;
   const int grid = num_sms * kCtasPerSm < kMaxDecodeCtas ? num_sms * kCtasPerSm : kMaxDecodeCtas;
   const DecodeWorkspace lay = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas);
   if (ws_bytes < lay.total) return PSW_EWORKSPACE;
@@ -642,13 +764,13 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   float* ws_o = reinterpret_cast<float*>(base + lay.o_offset);
   float2* ws_ml = reinterpret_cast<float2*>(base + lay.ml_offset);
   int32_t* tickets = reinterpret_cast<int32_t*>(base + lay.ticket_offset);
-  if (set_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<HD, KEQV>),
+  if (set_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<HD, KEQV, FP8>),
                      C::kSmemBytes) != PSW_OK)
     return PSW_ELAUNCH;
-  decode_split_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
+  decode_split_kernel<HD, KEQV, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(
       k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
       seq_lens, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.window, L.scale, L.softcap,
-      out, lse, ws_o, ws_ml, tickets, err);
+      out, lse, ws_o, ws_ml, tickets, k_scale, v_scale, err);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 
@@ -673,24 +795,20 @@ DecodeWorkspace decode_workspace_layout(const LayerArgs& L, int n_seqs, int max_
 int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
                   int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse,
-                  void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream) {
+                  void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream,
+                  const float* k_scale, const float* v_scale) {
   if (n_seqs == 0) return PSW_OK;
+  const bool fp8 = k_scale != nullptr;
+#define PSW_DEC(HD, KV, F8)                                                                  \
+  dec::launch<HD, KV, F8>(L, q, k_map, v_map, block_table, max_blocks, num_blocks, seq_lens, \
+                          n_seqs, out, lse, ws, ws_bytes, num_sms, err, stream, k_scale, v_scale)
   if (L.hd == 256) {
-    return L.k_eq_v
-               ? dec::launch<256, true>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
-                                        seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
-                                        stream)
-               : dec::launch<256, false>(L, q, k_map, v_map, block_table, max_blocks,
-                                         num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
-                                         num_sms, err, stream);
+    if (fp8) return L.k_eq_v ? PSW_DEC(256, true, true) : PSW_DEC(256, false, true);
+    return L.k_eq_v ? PSW_DEC(256, true, false) : PSW_DEC(256, false, false);
   }
-  return L.k_eq_v
-             ? dec::launch<512, true>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
-                                      seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
-                                      stream)
-             : dec::launch<512, false>(L, q, k_map, v_map, block_table, max_blocks, num_blocks,
-                                       seq_lens, n_seqs, out, lse, ws, ws_bytes, num_sms, err,
-                                       stream);
+  if (fp8) return L.k_eq_v ? PSW_DEC(512, true, true) : PSW_DEC(512, false, true);
+  return L.k_eq_v ? PSW_DEC(512, true, false) : PSW_DEC(512, false, false);
+#undef PSW_DEC
 }
 
 }  // namespace psw

@@ -66,11 +66,28 @@ cudaError_t launch_kv_cache_write(const LayerArgs& L, const void* k, const void*
                                   void* k_pool, void* v_pool, int num_sms, int32_t* err,
                                   cudaStream_t stream);
 
-// Returns a PSW_* code.
+// Returns a PSW_* code. With k_scale (FP8 pages), the maps are e4m3 pool maps
+// (make_pool_tensor_map_fp8) and k_scale / v_scale the per-row scales
+// (v_scale unused with k_eq_v).
 int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
-                  int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse, void* ws,
-                  size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream);
+                  int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse,
+                  void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream,
+                  const float* k_scale = nullptr, const float* v_scale = nullptr);
+
+// TMA descriptor of an e4m3 pool [num_blocks][16][n_kv][hd] (one byte per
+// value) seen as [slot][chunk of 64 codes][64], box = 16 slots x 1 chunk.
+int make_pool_tensor_map_fp8(CUtensorMap* map, const void* pool, int64_t num_blocks, int n_kv,
+                             int hd);
+
+// FP8 cache write: each (token, KV head) row quantised to e4m3 with one fp32
+// scale (amax / 448). v / v_pool8 / v_scale NULL with k_eq_v.
+cudaError_t launch_kv_cache_write_fp8(const LayerArgs& L, const void* k, const void* v,
+                                      const int32_t* cu_new, const int32_t* past_lens,
+                                      int n_seqs, const int32_t* block_table, int max_blocks,
+                                      int64_t num_blocks, void* k_pool8, void* v_pool8,
+                                      float* k_scale, float* v_scale, int num_sms, int32_t* err,
+                                      cudaStream_t stream);
 
 // Pre-attention step parameters after validation.
 struct NormRopeArgs {

@@ -106,3 +106,54 @@ class MixedLayerStep:
         binding.attn_prefill_chunked(L, self.pre_q, self.pre_cu, self.pre_past, self.max_chunk,
                                      g.k_pool, g.v_pool, self.pre_pages, self.pre_out,
                                      self.pre_lse, g.ws)
+
+
+FP8_CANARY = 0x7F  # an E4M3 NaN code: a read of a never-written slot shows
+
+
+class GpuStepFP8:
+    """A step on FP8 pages: e4m3 code pools (canary-filled), fp32 scale pools
+    (NaN-filled), the history written by the library's FP8 cache write."""
+
+    def __init__(self, step: wl.Step, device="cuda"):
+        self.step = step
+        layer = step.layer
+        c = step.cache
+        shape = c.pool_shape
+        self.k_pool8 = torch.full(shape, FP8_CANARY, dtype=torch.uint8, device=device)
+        self.k_scale = torch.full(shape[:3], float("nan"), dtype=torch.float32, device=device)
+        self.v_pool8 = None if layer.k_eq_v else torch.full(shape, FP8_CANARY, dtype=torch.uint8,
+                                                            device=device)
+        self.v_scale = None if layer.k_eq_v else torch.full(shape[:3], float("nan"),
+                                                            dtype=torch.float32, device=device)
+        self.table = dev_i32(step.block_table, device)
+        self.pages = binding.make_pages(self.table, c.num_blocks)
+        if c.hist_k.shape[0] > 0:
+            binding.kv_cache_write_fp8(layer, dev_bf16(c.hist_k, device),
+                                       None if layer.k_eq_v else dev_bf16(c.hist_v, device),
+                                       dev_i32(c.hist_cu, device), dev_i32(c.hist_past, device),
+                                       self.pages, self.k_pool8, self.v_pool8, self.k_scale,
+                                       self.v_scale)
+        self.q = dev_bf16(step.q, device)
+        self.new_k = dev_bf16(step.new_k, device)
+        self.new_v = None if layer.k_eq_v else dev_bf16(step.new_v, device)
+        self.cu_new = dev_i32(step.cu_new, device)
+        self.past = dev_i32(step.past_lens, device)
+        self.seq_lens = dev_i32(step.seq_lens, device)
+        n_rows = step.q.shape[0]
+        self.out = torch.full((n_rows, layer.n_q_heads, layer.head_dim), float("nan"),
+                              dtype=torch.float32, device=device)
+        self.lse = torch.full((n_rows, layer.n_q_heads), float("nan"), dtype=torch.float32,
+                              device=device)
+        max_len = int(step.seq_lens.max()) if step.n_seqs else 0
+        self.ws = binding.alloc_workspace(layer, step.n_seqs, max_len, device)
+
+    def write_new(self):
+        binding.kv_cache_write_fp8(self.step.layer, self.new_k, self.new_v, self.cu_new,
+                                   self.past, self.pages, self.k_pool8, self.v_pool8,
+                                   self.k_scale, self.v_scale)
+
+    def decode(self):
+        binding.attn_decode_paged_fp8(self.step.layer, self.q, self.k_pool8, self.v_pool8,
+                                      self.k_scale, self.v_scale, self.pages, self.seq_lens,
+                                      self.out, self.lse, self.ws)

@@ -266,3 +266,46 @@ def test_norm_rope_argument_checks(lib):
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
 def test_norm_rope_without_gpu_fails_loudly(lib):
     assert _norm_rope(lib, _layer()) == -13
+
+
+def _decode8(lib, layer, q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, pages=None, seq=FAKE, n=4,
+             out=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    pages = pages or _pages()
+    return lib.attn_decode_paged_fp8(ctypes.byref(layer), q, k, v, ks, vs, ctypes.byref(pages),
+                                     seq, n, out, None, ws, ws_bytes, None)
+
+
+def _write8(lib, layer, k=FAKE, v=FAKE, cu=FAKE, past=FAKE, n=4, pages=None, kp=FAKE, vp=FAKE,
+            ks=FAKE, vs=FAKE):
+    pages = pages or _pages()
+    return lib.kv_cache_write_fp8(ctypes.byref(layer), k, v, cu, past, n, ctypes.byref(pages),
+                                  kp, vp, ks, vs, None)
+
+
+def test_fp8_argument_checks(lib):
+    layer = _layer()
+    assert _decode8(lib, _layer(head_dim=128)) == -3
+    assert _write8(lib, _layer(head_dim=128)) == -3
+    assert _decode8(lib, layer, ks=None) == -1
+    assert _write8(lib, layer, ks=None) == -1
+    assert _decode8(lib, layer, vs=None) == -7           # V scales missing on a k_eq_v = 0 layer
+    assert _write8(lib, layer, vs=None) == -7
+    keqv = _layer(k_eq_v=1, n_q_heads=32, n_kv_heads=4, head_dim=512, window=0)
+    assert _decode8(lib, keqv, v=None) == -7             # V scales given on a k_eq_v layer
+    assert _decode8(lib, keqv, v=None, vs=None, n=0) == 0
+    assert _write8(lib, keqv, v=None, vp=None) == -7
+    assert _write8(lib, keqv, v=None, vp=None, vs=None, n=0) == 0
+    assert _decode8(lib, layer, ks=FAKE + 2) == -12      # scales: 4-byte aligned
+    assert _write8(lib, layer, vs=FAKE + 1) == -12
+    assert _write8(lib, layer, kp=FAKE + 8) == -12       # code pools: 16-byte aligned
+    assert _decode8(lib, layer, ws=None) == -10
+    assert _decode8(lib, layer, n=-1) == -9
+    assert _write8(lib, layer, n=-1) == -9
+    assert _decode8(lib, layer, n=0, ws=None, ws_bytes=0) == 0
+    assert _write8(lib, layer, n=0) == 0
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
+def test_fp8_without_gpu_fails_loudly(lib):
+    assert _decode8(lib, _layer()) == -13
+    assert _write8(lib, _layer()) == -13
