@@ -427,6 +427,23 @@ PSW_API int psw_get_error(psw_stream_t stream, int32_t *device_error_out);
 /* Static string describing a return code. */
 PSW_API const char *psw_strerror(int code);
 
+/*
+ * Testing hook for the bounded pipeline waits; not for production use.
+ * kernel 1 (attn_decode_paged, attn_decode_paged_fp8) or 2
+ * (attn_prefill_chunked): from the next launch of that kernel on, the TMA
+ * producer of CTA `cta` leaves its copy number `tile` (counted from 0 over its
+ * own K-tile copies) unissued and stops, without flagging anything. The
+ * consumer waiting for that copy then gives up after its bound (about one
+ * second), sets PSW_DEVERR_PIPELINE and abandons the CTA's remaining work;
+ * the producer still waits for every copy it did issue, and the prefill
+ * kernel still frees its tensor memory, before the CTA exits. Outputs of the
+ * abandoned work are left unwritten, and a decode call may leave the
+ * workspace's counter block non-zero (zero it before the next call). kernel 0
+ * switches the hook off. Returns PSW_OK, or PSW_EINVAL_NSEQS for a kernel
+ * outside [0, 2] or a negative cta or tile.
+ */
+PSW_API int psw_testing_stall(int32_t kernel, int32_t cta, int32_t tile);
+
 #ifdef __cplusplus
 }
 #endif

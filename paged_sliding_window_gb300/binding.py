@@ -33,7 +33,7 @@ EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
             "psw_block_pool_allocate", "psw_block_pool_free", "psw_block_pool_get_cached",
             "psw_block_pool_cache", "psw_block_pool_ref_count", "psw_block_hash",
             "psw_block_pool_admit", "psw_block_pool_commit", "kv_cache_write_fp8",
-            "attn_decode_paged_fp8")
+            "attn_decode_paged_fp8", "psw_testing_stall")
 
 
 class PswLayer(ctypes.Structure):
@@ -121,6 +121,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.attn_decode_paged_fp8.argtypes = [lp, vp, vp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz,
                                               vp]
         lib.attn_decode_paged_fp8.restype = ctypes.c_int
+        lib.psw_testing_stall.argtypes = [i32, i32, i32]
+        lib.psw_testing_stall.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
         lib.psw_strerror.argtypes = [ctypes.c_int]
         lib.psw_strerror.restype = ctypes.c_char_p
@@ -293,6 +295,15 @@ def attn_decode_paged_fp8(layer, q, k_pool8, v_pool8, k_scale, v_scale, pages: P
                                       int(seq_lens.shape[0]), _ptr(out), _ptr(lse), _ptr(ws),
                                       ws_bytes, _stream(stream))
     _raise(rc, "attn_decode_paged_fp8")
+
+
+STALL_OFF, STALL_DECODE, STALL_PREFILL = 0, 1, 2
+
+
+def testing_stall(kernel: int, cta: int = -1, tile: int = -1) -> None:
+    """Testing hook: CTA `cta` of the next launches of `kernel` leaves its
+    tile copy `tile` unissued, so a bounded wait runs out (STALL_OFF: off)."""
+    _raise(load().psw_testing_stall(kernel, cta, tile), "psw_testing_stall")
 
 
 def make_norm_rope(theta: float, partial_rotary_factor: float = 1.0, eps: float = 1e-6,

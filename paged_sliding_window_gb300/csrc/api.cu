@@ -142,6 +142,17 @@ int set_smem_limit(const void* kernel, int bytes) {
   return PSW_OK;
 }
 
+namespace {
+std::mutex g_stall_mutex;
+int g_stall_kernel = 0;
+StallHook g_stall;
+}  // namespace
+
+StallHook stall_hook(int kernel) {
+  std::lock_guard<std::mutex> lock(g_stall_mutex);
+  return g_stall_kernel == kernel ? g_stall : StallHook{};
+}
+
 int check_decode_args(const psw_layer_t* layer, const void* q, const void* k_pool,
                       const void* v_pool, const psw_pages_t* pages, const int32_t* seq_lens,
                       int32_t n_seqs, const float* out, LayerArgs* L) {
@@ -489,6 +500,15 @@ int psw_kv_share_map(int32_t n_layers, int32_t pattern, int32_t n_shared, int32_
     if (is_full != nullptr) is_full[i] = full;
     if (target != nullptr) target[i] = i < owners ? i : last_owner[full];
   }
+  return PSW_OK;
+}
+
+int psw_testing_stall(int32_t kernel, int32_t cta, int32_t tile) {
+  if (kernel < 0 || kernel > kStallPrefill) return PSW_EINVAL_NSEQS;
+  if (kernel != 0 && (cta < 0 || tile < 0)) return PSW_EINVAL_NSEQS;
+  std::lock_guard<std::mutex> lock(g_stall_mutex);
+  g_stall_kernel = kernel;
+  g_stall = kernel == 0 ? StallHook{} : StallHook{cta, tile};
   return PSW_OK;
 }
 

@@ -232,7 +232,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     float* __restrict__ lse, float* __restrict__ ws_o,
                     float2* __restrict__ ws_ml, int32_t* __restrict__ tickets,
                     const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                    int32_t* err) {
+                    int32_t* err, int stall_cta, int stall_tile) {
   using C = Cfg<HD, KEQV, FP8>;
   constexpr int TP = C::kTilePages;
   extern __shared__ uint8_t smem_raw[];
@@ -337,6 +337,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const int lc = lane % C::kChunks;
     int issued = 0;
     for (int t = t_begin; t < t_end; ++t, ++issued) {
+      // testing hook: this copy is never issued, so a consumer wait runs out
+      if (static_cast<int>(blockIdx.x) == stall_cta && issued == stall_tile) break;
       const int stage = issued % C::kStages;
       const uint32_t ph = (issued / C::kStages) & 1;
       const int kvh = w.unit / qchunks;
@@ -767,10 +769,11 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   if (set_smem_limit(reinterpret_cast<const void*>(decode_split_kernel<HD, KEQV, FP8>),
                      C::kSmemBytes) != PSW_OK)
     return PSW_ELAUNCH;
+  const StallHook stall = stall_hook(kStallDecode);
   decode_split_kernel<HD, KEQV, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(
       k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
       seq_lens, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.window, L.scale, L.softcap,
-      out, lse, ws_o, ws_ml, tickets, k_scale, v_scale, err);
+      out, lse, ws_o, ws_ml, tickets, k_scale, v_scale, err, stall.cta, stall.tile);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 

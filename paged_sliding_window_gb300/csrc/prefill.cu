@@ -406,7 +406,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
                int max_blocks, int64_t num_blocks, int n_q_total, int max_q_len, int n_q,
                int group, int window, float scale, float softcap, PlanHeader* hdr,
                const int2* __restrict__ units, float* __restrict__ out,
-               float* __restrict__ lse, int32_t* err) {
+               float* __restrict__ lse, int32_t* err, int stall_cta, int stall_tile) {
   using C = Cfg<HD, KEQV>;
   constexpr int BN = C::kBN;
   constexpr int KS = C::kKStages;
@@ -502,6 +502,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
     int nq = 0;     // Q tiles issued
     int n_fix = 0;  // V tiles that landed on v_fix
     bool ok = true;
+    bool stalled = false;  // testing hook: the K copy gt == stall_tile is never issued
     for (int n = 0; ok; ++n) {
       // ---- the item: the K warp takes it and publishes it, the V warp reads it
       int item = -1;
@@ -587,6 +588,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
           const uint32_t ph = static_cast<uint32_t>(gt / nst) & 1u;
           uint64_t* empty = v_side ? &bars->v_empty[stage] : &bars->k_empty[stage];
           uint64_t* full = v_side ? &bars->v_full[stage] : &bars->k_full[stage];
+          if (!v_side && static_cast<int>(blockIdx.x) == stall_cta && gt == stall_tile) {
+            stalled = true;  // leave quietly: the waits downstream must run out
+            ok = false;
+            break;
+          }
           if (lane == 0) ok = mbar_wait(empty, ph ^ 1) && !*abort_flag;
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
@@ -629,7 +635,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant_
         }
       }
     }
-    if (!ok && lane == 0) {
+    if (!ok && !stalled && lane == 0) {
       flag_error(err, PSW_DEVERR_PIPELINE);
       *abort_flag = 1;
     }
@@ -1144,9 +1150,11 @@ int launch(const LayerArgs& L, const CUtensorMap& q_map, const CUtensorMap& k_ma
   const int64_t max_items =
       static_cast<int64_t>(n_seqs) * max_rb * L.n_kv * C::kDSplit;
   const int grid = static_cast<int>(max_items < num_sms ? max_items : num_sms);
+  const StallHook stall = stall_hook(kStallPrefill);
   prefill_kernel<HD, KEQV><<<grid, kThreads, C::kSmemBytes, stream>>>(
       q_map, k_map, v_map, cu_q, past_lens, block_table, max_blocks, num_blocks, n_q_total,
-      max_q_len, L.n_q, L.group(), L.window, L.scale, L.softcap, hdr, units, out, lse, err);
+      max_q_len, L.n_q, L.group(), L.window, L.scale, L.softcap, hdr, units, out, lse, err,
+      stall.cta, stall.tile);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 

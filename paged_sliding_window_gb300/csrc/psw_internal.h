@@ -52,6 +52,14 @@ int32_t* device_error_word();
 // (kernel, device); safe to call from several host threads. Returns a PSW_* code.
 int set_smem_limit(const void* kernel, int bytes);
 
+// Testing hook set by psw_testing_stall: the CTA whose producer leaves tile
+// copy `tile` (counted from 0 over its own copies) unissued; -1: none.
+struct StallHook {
+  int cta = -1, tile = -1;
+};
+constexpr int kStallDecode = 1, kStallPrefill = 2;
+StallHook stall_hook(int kernel);
+
 // Decode workspace layout (bytes): merge tickets (counter block) | partial O |
 // partial (m, l).
 struct DecodeWorkspace {

@@ -309,3 +309,12 @@ def test_fp8_argument_checks(lib):
 def test_fp8_without_gpu_fails_loudly(lib):
     assert _decode8(lib, _layer()) == -13
     assert _write8(lib, _layer()) == -13
+
+
+def test_testing_stall_argument_checks(lib):
+    assert lib.psw_testing_stall(3, 0, 0) == -9
+    assert lib.psw_testing_stall(-1, 0, 0) == -9
+    assert lib.psw_testing_stall(1, -1, 0) == -9
+    assert lib.psw_testing_stall(2, 0, -1) == -9
+    assert lib.psw_testing_stall(1, 0, 2) == 0
+    assert lib.psw_testing_stall(0, -1, -1) == 0
