@@ -178,6 +178,30 @@ PSW_API int attn_decode_paged(const psw_layer_t *layer, const void *q, const voi
                       void *ws, size_t ws_bytes, psw_stream_t stream);
 
 /*
+ * One decode step in one launch: kv_cache_write of each sequence's new token
+ * followed by attn_decode_paged, fused. Sequence b's new K/V row (the query's
+ * own token, position seq_lens[b] - 1) is stored in its slot of the pools and
+ * attended to in the same pass: the kernel that stages the page holding it
+ * takes the row from k_new / v_new instead of the pool, so no second launch
+ * and no ordering between the two is needed. Results and pools equal those of
+ * kv_cache_write (cu_new = 0..n_seqs, past_lens = seq_lens - 1) then
+ * attn_decode_paged.
+ *   k_new, v_new  device bf16 [n_seqs][n_kv_heads][head_dim], 16-byte aligned;
+ *                 v_new NULL when k_eq_v
+ *   k_pool, v_pool  as attn_decode_paged, written at the new slots
+ * Every other argument, the workspace and the errors are those of
+ * attn_decode_paged (PSW_ENULL for a missing k_new; PSW_EINVAL_KEQV when
+ * v_new breaks the k_eq_v rule). A sequence of length 0 writes nothing; a
+ * new slot with a bad block id or beyond the table row is skipped and flagged
+ * as by kv_cache_write.
+ */
+PSW_API int attn_decode_paged_append(const psw_layer_t *layer, const void *q, const void *k_new,
+                                     const void *v_new, void *k_pool, void *v_pool,
+                                     const psw_pages_t *pages, const int32_t *seq_lens,
+                                     int32_t n_seqs, float *out, float *lse, void *ws,
+                                     size_t ws_bytes, psw_stream_t stream);
+
+/*
  * Chunked prefill: sequence b contributes the chunk rows
  * cu_q[b] <= t < cu_q[b+1]; row i = t - cu_q[b] sits at position
  * past_lens[b] + i and attends over keys [0, past_lens[b] + i] under the band

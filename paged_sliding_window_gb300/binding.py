@@ -33,7 +33,7 @@ EXPORTED = ("psw_workspace_bytes", "kv_cache_write", "attn_decode_paged",
             "psw_block_pool_allocate", "psw_block_pool_free", "psw_block_pool_get_cached",
             "psw_block_pool_cache", "psw_block_pool_ref_count", "psw_block_hash",
             "psw_block_pool_admit", "psw_block_pool_commit", "kv_cache_write_fp8",
-            "attn_decode_paged_fp8", "psw_testing_stall")
+            "attn_decode_paged_fp8", "psw_testing_stall", "attn_decode_paged_append")
 
 
 class PswLayer(ctypes.Structure):
@@ -121,6 +121,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.attn_decode_paged_fp8.argtypes = [lp, vp, vp, vp, vp, vp, pp, vp, i32, vp, vp, vp, sz,
                                               vp]
         lib.attn_decode_paged_fp8.restype = ctypes.c_int
+        lib.attn_decode_paged_append.argtypes = [lp, vp, vp, vp, vp, vp, pp, vp, i32, vp, vp, vp,
+                                                 sz, vp]
+        lib.attn_decode_paged_append.restype = ctypes.c_int
         lib.psw_testing_stall.argtypes = [i32, i32, i32]
         lib.psw_testing_stall.restype = ctypes.c_int
         lib.psw_get_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -257,6 +260,25 @@ def attn_decode_paged_noalloc(layer, q, k_pool, v_pool, pages: PswPages, seq_len
                                           _ptr(seq_lens), int(seq_lens.shape[0]), _ptr(out),
                                           _ptr(lse), _stream(stream))
     _raise(rc, "attn_decode_paged_noalloc")
+
+
+def attn_decode_paged_append(layer, q, k_new, v_new, k_pool, v_pool, pages: PswPages, seq_lens,
+                             out, lse=None, ws=None, stream=None) -> None:
+    """One decode step in one launch: each sequence's new K/V row written at
+    position seq_len - 1 and attended to (kv_cache_write + attn_decode_paged)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"),
+                 (v_pool, "v_pool")):
+        _check(t, torch.bfloat16, n)
+    _check(seq_lens, torch.int32, "seq_lens")
+    _check(out, torch.float32, "out")
+    _check(lse, torch.float32, "lse")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    rc = load().attn_decode_paged_append(ctypes.byref(make_layer(layer)), _ptr(q), _ptr(k_new),
+                                         _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                         ctypes.byref(pages), _ptr(seq_lens),
+                                         int(seq_lens.shape[0]), _ptr(out), _ptr(lse), _ptr(ws),
+                                         ws_bytes, _stream(stream))
+    _raise(rc, "attn_decode_paged_append")
 
 
 def kv_cache_write_fp8(layer, k, v, cu_new, past_lens, pages: PswPages, k_pool8, v_pool8,

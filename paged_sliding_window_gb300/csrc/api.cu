@@ -324,6 +324,42 @@ int attn_decode_paged(const psw_layer_t* layer, const void* q, const void* k_poo
                        st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int attn_decode_paged_append(const psw_layer_t* layer, const void* q, const void* k_new,
+                             const void* v_new, void* k_pool, void* v_pool,
+                             const psw_pages_t* pages, const int32_t* seq_lens, int32_t n_seqs,
+                             float* out, float* lse, void* ws, size_t ws_bytes,
+                             psw_stream_t stream) {
+  LayerArgs L;
+  int rc = check_decode_args(layer, q, k_pool, v_pool, pages, seq_lens, n_seqs, out, &L);
+  if (rc != PSW_OK) return rc;
+  if (k_new == nullptr) return PSW_ENULL;
+  if ((rc = check_v(L, v_new)) != PSW_OK) return rc;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PSW_EALIGN;
+  if (n_seqs == 0) return PSW_OK;
+  if (ws == nullptr) return PSW_EWORKSPACE;
+  if (ws_bytes < decode_workspace_layout(L, n_seqs, kMaxDecodeCtas).total) return PSW_EWORKSPACE;
+  DeviceState* st;
+  if ((rc = device_ready(&st)) != PSW_OK) return rc;
+  CUtensorMap k_map, v_map;
+  if ((rc = make_pool_tensor_map(&k_map, k_pool, pages->num_blocks, L.n_kv, L.hd)) != PSW_OK)
+    return rc;
+  if (L.k_eq_v) {
+    v_map = k_map;
+  } else if ((rc = make_pool_tensor_map(&v_map, v_pool, pages->num_blocks, L.n_kv, L.hd)) !=
+             PSW_OK) {
+    return rc;
+  }
+  AppendArgs app;
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.k_pool = k_pool;
+  app.v_pool = v_pool;
+  return launch_decode(L, q, k_map, v_map, pages->block_table, pages->max_blocks_per_seq,
+                       pages->num_blocks, seq_lens, n_seqs, out, lse, ws, ws_bytes,
+                       st->info.num_sms, st->err, reinterpret_cast<cudaStream_t>(stream),
+                       nullptr, nullptr, app);
+}
+
 namespace {
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 }  // namespace

@@ -232,7 +232,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                     float* __restrict__ lse, float* __restrict__ ws_o,
                     float2* __restrict__ ws_ml, int32_t* __restrict__ tickets,
                     const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                    int32_t* err, int stall_cta, int stall_tile) {
+                    int32_t* err, int stall_cta, int stall_tile, AppendArgs append) {
   using C = Cfg<HD, KEQV, FP8>;
   constexpr int TP = C::kTilePages;
   extern __shared__ uint8_t smem_raw[];
@@ -489,6 +489,45 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     if (!landed && lane == 0) {
       flag_error(err, PSW_DEVERR_PIPELINE);
       *cons_abort = 1;
+    }
+    // Append mode: this unit's last tile holds the step's new token
+    // (position len - 1); its K/V rows come from the inputs into this warp's
+    // chunks of the staged tile (each warp reads only its own chunks), and
+    // the unit of the first query chunk also stores them in the pools for
+    // later steps. A bad block id or length was flagged by the producer or
+    // the prologue; such a row is left alone.
+    if constexpr (!FP8) {
+      if (append.k_new != nullptr && landed && w.tile == w.ntu - 1 && w.len > 0 &&
+          seq_lens[w.s] == w.len) {
+        const int pos = w.len - 1, page = pos / kBlockSize, row = pos % kBlockSize;
+        const int kk = page - page0;
+        const int kvh = w.unit / qchunks;
+        const int32_t blk = page < max_blocks
+                                ? block_table[static_cast<int64_t>(w.s) * max_blocks + page]
+                                : -1;
+        if (blk >= 0 && blk < num_blocks) {
+          const bool to_pool = w.unit == kvh * qchunks;
+          constexpr int kUnits = C::kChunksPerWarp * 8;  // 16-byte units of this warp's dims
+          uint8_t* tile = stages + stage * C::kStageBytes + kk * C::kPageBytes;
+          const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + row;
+          for (int idx = lane; idx < (KEQV ? 1 : 2) * kUnits; idx += 32) {
+            const int which = idx / kUnits, rem = idx - which * kUnits;
+            const int c = warp * C::kChunksPerWarp + rem / 8, u = rem & 7;
+            const int d = c * 64 + u * 8;
+            const uint4 val = *reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(which ? append.v_new : append.k_new) +
+                (static_cast<int64_t>(w.s) * n_kv + kvh) * HD + d);
+            *reinterpret_cast<uint4*>(tile + which * C::kKTileBytes + c * kChunkBytes + row * 128 +
+                                      ((u ^ (row & 7)) << 4)) = val;
+            if (to_pool)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? append.v_pool
+                                                                           : append.k_pool) +
+                                        (slot * n_kv + kvh) * HD + d) = val;
+          }
+          fence_proxy_async_smem();  // the stage is later refilled by TMA
+          __syncwarp();
+        }
+      }
     }
     // FP8: this warp converts its quarter of head_dim of the tile (K, and V
     // unless k_eq_v) into the bf16 tile, keeps the scales of its keys (same
@@ -757,7 +796,8 @@ template <int HD, bool KEQV, bool FP8>
 int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CUtensorMap& v_map,
            const int32_t* block_table, int max_blocks, int64_t num_blocks, const int32_t* seq_lens,
            int n_seqs, float* out, float* lse, void* ws, size_t ws_bytes, int num_sms,
-           int32_t* err, cudaStream_t stream, const float* k_scale, const float* v_scale) {
+           int32_t* err, cudaStream_t stream, const float* k_scale, const float* v_scale,
+           AppendArgs append) {
   using C = Cfg<HD, KEQV, FP8>;
   const int grid = num_sms * kCtasPerSm < kMaxDecodeCtas ? num_sms * kCtasPerSm : kMaxDecodeCtas;
   const DecodeWorkspace lay = decode_workspace_layout(L, n_seqs, kMaxDecodeCtas);
@@ -773,7 +813,7 @@ int launch(const LayerArgs& L, const void* q, const CUtensorMap& k_map, const CU
   decode_split_kernel<HD, KEQV, FP8><<<grid, kThreads, C::kSmemBytes, stream>>>(
       k_map, v_map, static_cast<const __nv_bfloat16*>(q), block_table, max_blocks, num_blocks,
       seq_lens, n_seqs, L.n_q, L.n_kv, L.group(), L.qchunks(), L.window, L.scale, L.softcap,
-      out, lse, ws_o, ws_ml, tickets, k_scale, v_scale, err, stall.cta, stall.tile);
+      out, lse, ws_o, ws_ml, tickets, k_scale, v_scale, err, stall.cta, stall.tile, append);
   return cudaGetLastError() == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 
@@ -799,12 +839,13 @@ int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
                   int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse,
                   void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream,
-                  const float* k_scale, const float* v_scale) {
+                  const float* k_scale, const float* v_scale, AppendArgs append) {
   if (n_seqs == 0) return PSW_OK;
   const bool fp8 = k_scale != nullptr;
 #define PSW_DEC(HD, KV, F8)                                                                  \
   dec::launch<HD, KV, F8>(L, q, k_map, v_map, block_table, max_blocks, num_blocks, seq_lens, \
-                          n_seqs, out, lse, ws, ws_bytes, num_sms, err, stream, k_scale, v_scale)
+                          n_seqs, out, lse, ws, ws_bytes, num_sms, err, stream, k_scale, v_scale, \
+                          append)
   if (L.hd == 256) {
     if (fp8) return L.k_eq_v ? PSW_DEC(256, true, true) : PSW_DEC(256, false, true);
     return L.k_eq_v ? PSW_DEC(256, true, false) : PSW_DEC(256, false, false);

@@ -74,14 +74,26 @@ cudaError_t launch_kv_cache_write(const LayerArgs& L, const void* k, const void*
                                   void* k_pool, void* v_pool, int num_sms, int32_t* err,
                                   cudaStream_t stream);
 
+// Append mode of the decode (attn_decode_paged_append): the step's new K/V
+// row of each sequence (k_new / v_new [n_seqs][n_kv][hd] bf16) is written to
+// its slot at position seq_len - 1 of the pools and used in place of that
+// slot's staged copy. All NULL: plain decode.
+struct AppendArgs {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+};
+
 // Returns a PSW_* code. With k_scale (FP8 pages), the maps are e4m3 pool maps
 // (make_pool_tensor_map_fp8) and k_scale / v_scale the per-row scales
-// (v_scale unused with k_eq_v).
+// (v_scale unused with k_eq_v). `append` is for bf16 pages only.
 int launch_decode(const LayerArgs& L, const void* q, const CUtensorMap& k_map,
                   const CUtensorMap& v_map, const int32_t* block_table, int max_blocks,
                   int64_t num_blocks, const int32_t* seq_lens, int n_seqs, float* out, float* lse,
                   void* ws, size_t ws_bytes, int num_sms, int32_t* err, cudaStream_t stream,
-                  const float* k_scale = nullptr, const float* v_scale = nullptr);
+                  const float* k_scale = nullptr, const float* v_scale = nullptr,
+                  AppendArgs append = AppendArgs{});
 
 // TMA descriptor of an e4m3 pool [num_blocks][16][n_kv][hd] (one byte per
 // value) seen as [slot][chunk of 64 codes][64], box = 16 slots x 1 chunk.

@@ -64,6 +64,13 @@ class GpuStep:
         binding.attn_decode_paged(self.step.layer, self.q, self.k_pool, self.v_pool, self.pages,
                                   self.seq_lens, self.out, self.lse, self.ws)
 
+    def decode_append(self):
+        """The fused step: writes the new rows and decodes (one new token per
+        sequence, as in a decode step)."""
+        binding.attn_decode_paged_append(self.step.layer, self.q, self.new_k, self.new_v,
+                                         self.k_pool, self.v_pool, self.pages, self.seq_lens,
+                                         self.out, self.lse, self.ws)
+
     def prefill(self):
         max_q = int(self.step.new_lens.max()) if self.step.n_seqs else 0
         binding.attn_prefill_chunked(self.step.layer, self.q, self.cu_new, self.past, max_q,

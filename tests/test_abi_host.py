@@ -318,3 +318,31 @@ def test_testing_stall_argument_checks(lib):
     assert lib.psw_testing_stall(2, 0, -1) == -9
     assert lib.psw_testing_stall(1, 0, 2) == 0
     assert lib.psw_testing_stall(0, -1, -1) == 0
+
+
+def _append(lib, layer, q=FAKE, kn=FAKE, vn=FAKE, k=FAKE, v=FAKE, pages=None, seq=FAKE, n=4,
+            out=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    pages = pages or _pages()
+    return lib.attn_decode_paged_append(ctypes.byref(layer), q, kn, vn, k, v,
+                                        ctypes.byref(pages), seq, n, out, None, ws, ws_bytes, None)
+
+
+def test_append_argument_checks(lib):
+    layer = _layer()
+    assert _append(lib, _layer(head_dim=128)) == -3
+    assert _append(lib, layer, kn=None) == -1
+    assert _append(lib, layer, q=None) == -1
+    assert _append(lib, layer, vn=None) == -7          # new V rows missing on a k_eq_v = 0 layer
+    keqv = _layer(k_eq_v=1, n_q_heads=32, n_kv_heads=4, head_dim=512, window=0)
+    assert _append(lib, keqv, v=None) == -7            # new V rows given on a k_eq_v layer
+    assert _append(lib, keqv, v=None, vn=None, n=0) == 0
+    assert _append(lib, layer, kn=FAKE + 8) == -12
+    assert _append(lib, layer, vn=FAKE + 2) == -12
+    assert _append(lib, layer, ws=None) == -10
+    assert _append(lib, layer, n=-1) == -9
+    assert _append(lib, layer, n=0, ws=None, ws_bytes=0) == 0
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
+def test_append_without_gpu_fails_loudly(lib):
+    assert _append(lib, _layer()) == -13
