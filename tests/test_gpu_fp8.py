@@ -83,6 +83,7 @@ EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 1000]
     pytest.param(Layer(8, 2, 512, window=48), id="hd512-g4-w48"),
     pytest.param(Layer(4, 4, 256, window=0, k_eq_v=True, scale=0.5), id="hd256-g1-keqv"),
     pytest.param(Layer(16, 2, 512, window=200, softcap=20.0), id="hd512-g8-w200-cap"),
+    pytest.param(Layer(32, 2, 256, window=0), id="hd256-g16-two-query-chunks"),
 ])
 def test_fp8_decode_edge_lengths(orc, layer):
     lens = np.array(EDGE_LENS)
