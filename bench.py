@@ -48,6 +48,7 @@ PROFILE_DECODE = ("decode_split_sliding_decode_batch.md", ("decode.cu", "ptx.cuh
 PROFILE_PREFILL = ("prefill_chunked_prefill_softcap.md", ("prefill.cu", "ptx.cuh"))
 PROFILE_FULL_DECODE = ("decode_split_full_keqv_decode.md", ("decode.cu", "ptx.cuh"))
 PROFILE_MIXED_PREFILL = ("prefill_mixed_step_full_layer.md", ("prefill.cu", "ptx.cuh"))
+PROFILE_PRE_ATTENTION = ("qkv_norm_rope_chunked_prefill.md", ("norm_rope.cu", "ptx.cuh"))
 L2_BYTES = 129 * 1024 * 1024
 # kv_cache_write_kernel, decode_split_kernel
 LAUNCHES_PER_STEP = 1
@@ -567,7 +568,13 @@ def measure_pre_attention(steps, warmup, hbm, peak_kind):
                      "value": gbs, "unit": "GB/s",
                      "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_kernel<256>",
                                   "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                                  "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": None}}
+                                  "frac": gbs / hbm, "peak_kind": peak_kind,
+                                  "traffic": (profiled_traffic(PROFILE_PRE_ATTENTION)
+                                              if name == "chunked_prefill" else None),
+                                  "traffic_source": "committed ncu summary (DRAM read + write "
+                                                    "per launch; the written rows stay in L2 "
+                                                    "within the call), null once the kernel "
+                                                    "source changed"}}
         del g
     return {"workload": "fused pre-attention step (q/k/v RMS-norm, RoPE, cache write)",
             "l2": "flushed (256 MB read) before every timed call", **res,
