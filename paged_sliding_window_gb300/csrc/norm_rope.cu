@@ -52,7 +52,15 @@ constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2 pi - kTwoPiHi
 // exponentials on it.
 struct FreqTable {
   double f[256];
+  float2 f2[256];  // the same split into a float and the float of the rest
 };
+
+// 2 pi in three floats (each the float nearest to what the previous ones
+// leave) and 1 / (2 pi) rounded to float, for the angle reduction below.
+constexpr float kC1 = 6.2831854820251465f;
+constexpr float kC2 = -1.7484555314695172e-7f;
+constexpr float kC3 = -6.8604980400235275e-15f;
+constexpr float kInvTwoPi = 0.15915493667125702f;
 
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -164,10 +172,25 @@ qkv_norm_rope_kernel(const __grid_constant__ FreqTable freq, const __nv_bfloat16
     for (int i = tid; i < kHalf; i += C::kThreads) {
       float c = 1.f, sn = 0.f;
       if (pos >= 0 && i < rope_angles) {
-        const double a = static_cast<double>(pos) * freq.f[i];
-        const double n = rint(a * (1.0 / kTwoPiHi));
-        const double r = fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, a));  // |r| <= pi
-        sincosf(static_cast<float>(r), &sn, &c);
+        float r;
+        if (pos < (1 << 24)) {
+          // pos f = ph + pl from the float parts of f (pos is exact in a
+          // float, ph's rounding error comes back exactly from the FMA), then
+          // Cody-Waite reduction by the three-float 2 pi: each FMA multiplies
+          // exactly and rounds once, so |r - (pos f mod 2 pi)| stays below
+          // about 4e-7 for f <= 1
+          const float pf = static_cast<float>(pos);
+          const float2 fq = freq.f2[i];
+          const float ph = pf * fq.x;
+          const float pl = fmaf(pf, fq.y, fmaf(pf, fq.x, -ph));
+          const float n = rintf(ph * kInvTwoPi);
+          r = fmaf(-n, kC3, fmaf(-n, kC2, fmaf(-n, kC1, ph))) + pl;
+        } else {  // beyond 2^24 the product needs double
+          const double a = static_cast<double>(pos) * freq.f[i];
+          const double n = rint(a * (1.0 / kTwoPiHi));
+          r = static_cast<float>(fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, a)));  // |r| <= pi
+        }
+        sincosf(r, &sn, &c);
       }
       st.cs[0][i] = make_float2(c, -sn);
       st.cs[1][i] = make_float2(c, sn);
@@ -323,10 +346,13 @@ int launch_qkv_norm_rope(const LayerArgs& L, const NormRopeArgs& R, const void* 
                          int32_t* err, cudaStream_t stream) {
   FreqTable ft;
   const double log_theta = log(static_cast<double>(R.theta));
-  for (int i = 0; i < 256; ++i)
+  for (int i = 0; i < 256; ++i) {
     ft.f[i] = (i < L.hd / 2 && i < R.rope_angles)
                   ? exp(-2.0 * static_cast<double>(i) / L.hd * log_theta)
                   : 0.0;
+    const float hi = static_cast<float>(ft.f[i]);
+    ft.f2[i] = make_float2(hi, static_cast<float>(ft.f[i] - static_cast<double>(hi)));
+  }
   const int nvec = L.n_q + (k != nullptr ? L.n_kv : 0) + (v != nullptr ? L.n_kv : 0);
   // 8 warps (16 at head_dim 512), each holding up to 4 head vectors of a
   // token per stage
