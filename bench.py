@@ -566,7 +566,7 @@ def measure_pre_attention(steps, warmup, hbm, peak_kind):
         gbs = nbytes / (ms / 1e3) / 1e9
         res[name] = {"tokens": n_tok, "ms_per_call": ms, "bytes_per_call": nbytes,
                      "value": gbs, "unit": "GB/s",
-                     "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_kernel<256>",
+                     "roofline": {"bound": "hbm", "kernel": "qkv_norm_rope_kernel<256, 4>",
                                   "achieved": gbs, "peak": hbm, "unit": "GB/s",
                                   "frac": gbs / hbm, "peak_kind": peak_kind,
                                   "traffic": (profiled_traffic(PROFILE_PRE_ATTENTION)

@@ -308,9 +308,10 @@ typedef struct {
  * normalised) is a k_eq_v = 0 layer that passes the same raw k buffer as v.
  * A layer that reads another layer's cache (KV sharing) passes k = v =
  * k_pool = v_pool = NULL (and may pass pages = NULL): only q is processed.
- * Errors: those of kv_cache_write, PSW_EINVAL_ROPE, PSW_ENULL for a missing
- * rn, q or q_out, and PSW_EINVAL_HEADS when one token's rows (n_q_heads +
- * 2 n_kv_heads head vectors) exceed 160 KB. Device-side errors are flagged
+ * Errors: those of kv_cache_write, PSW_EINVAL_ROPE and PSW_ENULL for a
+ * missing rn, q or q_out (any number of heads per token is accepted: the
+ * kernel takes a token's head vectors eight at a time, four at head_dim
+ * 512). Device-side errors are flagged
  * as by kv_cache_write: a token whose block id or capacity is wrong still
  * gets its q_out rows (only its K/V write is skipped); a token with an
  * invalid length or offsets is skipped.

@@ -16,25 +16,35 @@
 // on full ones. The normalised K and V rows go straight into their slots,
 // block_table[b][pos / 16] * 16 + pos % 16 (section 6.3 of that page).
 //
-// Design (how, on sm_103a): the kernel is HBM-bound on a prefill-sized step
-// and latency-bound on a decode step, and what costs time is the chain of
-// dependent steps per token (find the sequence, read its past length and
-// block id, form the angles), not arithmetic. A CTA (8 warps, 16 at
-// head_dim 512; about one wave of them) owns tokens t, t + grid, ... It
-// resolves up to 256 of them at once, thread j taking the j-th (sequence by
-// binary search over the offsets staged in shared memory, position, slot),
-// then runs them as a two-stage pipeline: while token j is computed, the
-// rows of token j + 1 are in flight (each warp loads up to four head
-// vectors, 16 or 32 bytes per lane each); its angles are formed at the
-// barrier between the two. An angle is pos * freq reduced to [-pi, pi] in
-// double, from frequencies the host computed in double (a float product
-// would lose about 0.006 rad at position 65536, far more than a bf16 unit),
-// with its sine and cosine in float. Computing a head vector: the sum of
-// squares reduced with shuffles, the norm's scale and weight, the rotation
-// of q and k (the partner of lane l's elements is held by lane l ^ 16: lanes
-// 0-15 hold the first half of the head, 16-31 the second), one rounding to
-// bf16, 16-byte stores to q_out or into the token's page slot.
+// Design (how, on sm_103a): the step is HBM-bound on a prefill-sized batch
+// and latency-bound on a decode batch; no block-wide barrier sits on its
+// path. A unit is NH head vectors of one tensor of one token (NH = 4, 2 or 1
+// at head_dim 256, the largest dividing both head counts; 1 at head_dim
+// 512), so every unit is full and one code path serves them all. Each warp
+// of a persistent grid (as many CTAs as fit on the SMs) takes a contiguous
+// block of units in token order, so consecutive units mostly share a token
+// whose position, page slot and rotation it keeps. Two register buffers
+// hold rows: the next unit's loads are in flight while one is processed.
+// The sequence of a token is found by the whole warp, which splits the
+// offsets 31 ways per round of coalesced loads (one round up to 31
+// sequences, two up to 961), reading past_lens in the last round. Lane l
+// holds elements [l m, l m + m) of each half of a head vector (m =
+// head_dim / 64), so the two elements of every rotation pair sit in the
+// same lane: the lane forms the rotation of its m pairs once per token and
+// rotates without shuffles. An angle is pos * freq reduced to [-pi/4, pi/4]
+// and a quadrant: below position 2^24 in float, from the two-float split of
+// a frequency the host computed in double, by Cody-Waite with a three-float
+// pi / 2 (plus a second step for the rounding of the quadrant above 2^22),
+// in double beyond; its sine and cosine from Taylor polynomials and the
+// quadrant's symmetry, 2.2e-7 at most in all. The sums of squares of a
+// unit's rows are reduced together (one halving shuffle tree, one
+// reciprocal square root per lane); the norm's weight and the rotation are
+// folded into per-element coefficients; one rounding to bf16; 8- or
+// 16-byte stores to q_out or into the token's page slot.
 #include <math.h>
+
+#include <atomic>
+#include <type_traits>
 
 #include "psw_internal.h"
 #include "ptx.cuh"
@@ -42,10 +52,7 @@
 namespace psw {
 namespace {
 
-constexpr int kNrStaged = 1024;  // cu_new entries staged in shared memory
-constexpr int kNrChunk = 256;    // tokens of a CTA resolved together
-constexpr double kTwoPiHi = 6.283185307179586;       // 2 pi rounded to double
-constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2 pi - kTwoPiHi
+constexpr int kThreads = 256;  // 8 warps per CTA, each on its own units
 
 // theta^(-2i / head_dim) for the rotated pairs, 0 beyond: computed on the host
 // in double and passed by value, so no CTA spends double-precision
@@ -55,39 +62,162 @@ struct FreqTable {
   float2 f2[256];  // the same split into a float and the float of the rest
 };
 
-// 2 pi in three floats (each the float nearest to what the previous ones
-// leave) and 1 / (2 pi) rounded to float, for the angle reduction below.
-constexpr float kC1 = 6.2831854820251465f;
-constexpr float kC2 = -1.7484555314695172e-7f;
-constexpr float kC3 = -6.8604980400235275e-15f;
-constexpr float kInvTwoPi = 0.15915493667125702f;
+// pi / 2 in three floats (each the float nearest to what the previous ones
+// leave; a quarter of the same split of 2 pi, exact in binary) and 2 / pi
+// rounded to float, for the angle reduction below.
+constexpr float kP1 = 1.5707963705062866f;
+constexpr float kP2 = -4.3711388286737929e-8f;
+constexpr float kP3 = -1.7151245100058819e-15f;
+constexpr float kTwoOverPi = 0.63661974668502808f;
+constexpr double kHalfPiHi = 1.5707963267948966;      // pi / 2 rounded to double
+constexpr double kHalfPiLo = 6.123233995736766e-17;   // pi / 2 - kHalfPiHi
 
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Per-token state of one pipeline stage: the token, its position and slot,
-// its rotation (cos, sin) per pair.
+// sin and cos of x + qd pi / 2 for |x| <= pi / 4 (a little beyond after
+// rounding): the Taylor series of sin through x^9 and of cos through x^8
+// (truncation below 1.8e-9 and 2.5e-8 at pi / 4), then the quadrant's
+// symmetry: (sin, cos) of x + pi / 2 is (cos x, -sin x), of x + pi is
+// (-sin x, -cos x), of x + 3 pi / 2 is (-cos x, sin x).
+__device__ __forceinline__ void sincos_quadrant(float x, int qd, float& sn, float& cs) {
+  const float x2 = x * x;
+  float sp = fmaf(x2, 1.f / 362880.f, -1.f / 5040.f);
+  sp = fmaf(x2, sp, 1.f / 120.f);
+  sp = fmaf(x2, sp, -1.f / 6.f);
+  const float sx = fmaf(x * x2, sp, x);
+  float cp = fmaf(x2, 1.f / 40320.f, -1.f / 720.f);
+  cp = fmaf(x2, cp, 1.f / 24.f);
+  cp = fmaf(x2, cp, -0.5f);
+  const float cx = fmaf(x2, cp, 1.f);
+  const float s0 = (qd & 1) ? cx : sx;
+  const float c0 = (qd & 1) ? sx : cx;
+  sn = __uint_as_float(__float_as_uint(s0) ^ ((qd & 2) ? 0x80000000u : 0u));
+  cs = __uint_as_float(__float_as_uint(c0) ^ (((qd + 1) & 2) ? 0x80000000u : 0u));
+}
+
+// bf16 -> float of the low and high half of a word by byte permutes, as
+// volatile asm: the rows are unpacked once for the sums of squares and again
+// for the results, and the second unpack must not be merged with the first
+// (that would keep every unpacked row live across the reduction).
+__device__ __forceinline__ float2 unpack_again(uint32_t w) {
+  uint32_t lo, hi;
+  asm volatile("prmt.b32 %0, %2, 0, 0x1044;\n\tprmt.b32 %1, %2, 0, 0x3244;"
+               : "=r"(lo), "=r"(hi)
+               : "r"(w));
+  return make_float2(__uint_as_float(lo), __uint_as_float(hi));
+}
+
+// A lane's share of one half of a head vector: HD / 64 bf16 values, one
+// 8-byte (head_dim 256) or 16-byte (head_dim 512) access.
 template <int HD>
-struct TokenStage {
-  // (cos, -sin) for the first half of the head, (cos, sin) for the second:
-  // out = y cos + partner * (signed sin) on either side
-  float2 cs[2][HD / 2];
-  long long slot;  // K/V slot, -1: no cache write
-  int pos;         // -1: token skipped
+struct Share;
+template <>
+struct Share<256> {
+  using T = uint2;
+  __device__ static void unpack(const T& r, float (&y)[4]) {
+    y[0] = __uint_as_float(r.x << 16);
+    y[1] = __uint_as_float(r.x & 0xFFFF0000u);
+    y[2] = __uint_as_float(r.y << 16);
+    y[3] = __uint_as_float(r.y & 0xFFFF0000u);
+  }
+  __device__ static void unpack_again(const T& r, float (&y)[4]) {
+    const float2 a = psw::unpack_again(r.x), b = psw::unpack_again(r.y);
+    y[0] = a.x, y[1] = a.y, y[2] = b.x, y[3] = b.y;
+  }
+  __device__ static T pack(const float (&y)[4]) {
+    return make_uint2(pack_bf16_rn(y[0], y[1]), pack_bf16_rn(y[2], y[3]));
+  }
+};
+template <>
+struct Share<512> {
+  using T = uint4;
+  __device__ static void unpack(const T& r, float (&y)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y[2 * e] = __uint_as_float(w[e] << 16);
+      y[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+  __device__ static void unpack_again(const T& r, float (&y)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = psw::unpack_again(w[e]);
+      y[2 * e] = a.x, y[2 * e + 1] = a.y;
+    }
+  }
+  __device__ static T pack(const float (&y)[8]) {
+    return make_uint4(pack_bf16_rn(y[0], y[1]), pack_bf16_rn(y[2], y[3]),
+                      pack_bf16_rn(y[4], y[5]), pack_bf16_rn(y[6], y[7]));
+  }
 };
 
-template <int HD, int WARPS, int ITEMS>
-struct NormRope {
-  static constexpr int kThreads = WARPS * 32;
-  static constexpr int kHalf = HD / 2;
-  static constexpr int kPer = HD / 32;    // elements per lane
-  static constexpr int kVecs = kPer / 8;  // 16-byte accesses per lane per vector
-};
+// Warp sums of VB values at once (x[j]: this lane's part of sum j). Each
+// round halves the list: a lane keeps one half, sends the other to its
+// partner across lane bit 16, 8, ... and adds what it receives; after
+// log2(VB) rounds lane l holds a partial of sum l / (32 / VB), which the
+// remaining xor rounds complete. VB - 1 + 5 - log2(VB) shuffles in all.
+template <int VB>
+__device__ __forceinline__ float warp_sums(float (&x)[VB], int lane) {
+#pragma unroll
+  for (int r = 0; (VB >> r) > 1; ++r) {
+    const int n = VB >> r, mask = 16 >> r;
+    const bool up = (lane & mask) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? x[i + n / 2] : x[i];
+      const float send = up ? x[i] : x[i + n / 2];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+    }
+  }
+  float m = x[0];
+#pragma unroll
+  for (int mask = 16 / VB; mask > 0; mask >>= 1) m += __shfl_xor_sync(0xffffffffu, m, mask);
+  return m;  // the sum number lane / (32 / VB)
+}
 
-template <int HD, int WARPS, int ITEMS>
-__global__ void __launch_bounds__(WARPS * 32)
+// The sequence of token t, found by the whole warp: b is the largest index
+// below n_seqs with cu_new[b] <= t. Each round the lanes probe the open range
+// at 31 evenly spaced offsets (one coalesced load), and the ballot of
+// "offset <= t" narrows it to one stride; the last round (range of at most
+// 31) probes every index plus the range's end, so it also yields
+// cu_new[b + 1], and it reads past_lens alongside. False when t lies before
+// cu_new[0] or outside [cu_new[b], cu_new[b + 1]) (offsets not monotone).
+// Every lane returns the same values.
+__device__ __forceinline__ bool find_sequence(const int32_t* __restrict__ cu_new,
+                                              const int32_t* __restrict__ past_lens,
+                                              int n_seqs, int t, int lane, int& b, int& start,
+                                              int& end, int& past) {
+  int lo = 0, hi = n_seqs;  // b in [lo, hi)
+  while (hi > lo) {
+    const int step = (hi - lo + 30) / 31;
+    const int idx = lo + lane * step;
+    const int c = idx <= hi ? __ldg(cu_new + idx) : 0;
+    const int pl = (step == 1 && idx < hi) ? __ldg(past_lens + idx) : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, idx < hi && c <= t);
+    if (m == 0) return false;
+    const int h = 31 - __clz(static_cast<int>(m));
+    if (step == 1) {  // h <= 30: lane h + 1 holds cu_new[b + 1]
+      b = lo + h;
+      start = __shfl_sync(0xffffffffu, c, h);
+      end = __shfl_sync(0xffffffffu, c, h + 1);
+      past = __shfl_sync(0xffffffffu, pl, h);
+      return t < end;
+    }
+    lo += h * step;
+    hi = min(hi, lo + step);
+  }
+  return false;
+}
+
+// NH head vectors of one tensor of one token form a unit; the host picks NH
+// so that every unit is full (a power of two dividing n_q and n_kv).
+template <int HD, int NH>
+__global__ void __launch_bounds__(kThreads, 2)  // two CTAs per SM: 128 registers
 qkv_norm_rope_kernel(const __grid_constant__ FreqTable freq, const __nv_bfloat16* q,
                      const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
                      const int32_t* __restrict__ cu_new, const int32_t* __restrict__ past_lens,
@@ -98,243 +228,248 @@ qkv_norm_rope_kernel(const __grid_constant__ FreqTable freq, const __nv_bfloat16
                      __nv_bfloat16* q_out,  // may be q itself: each lane rewrites what it read
                      __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ v_pool,
                      int32_t* err) {
-  using C = NormRope<HD, WARPS, ITEMS>;
-  constexpr int kPer = C::kPer, kVecs = C::kVecs, kHalf = C::kHalf;
-  __shared__ int32_t s_cu[kNrStaged];
-  __shared__ TokenStage<HD> s_st[2];
-  __shared__ long long s_slots[kNrChunk];  // the CTA's next kNrChunk tokens: slot
-  __shared__ int s_poss[kNrChunk];         // and position (-1: skipped)
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool staged = n_seqs < kNrStaged;  // uniform over the grid
-  if (staged)
-    for (int i = tid; i <= n_seqs; i += C::kThreads) s_cu[i] = cu_new[i];
+  constexpr int kM = HD / 64;  // elements of each half per lane
+  using S = Share<HD>;
+  using Vec = typename S::T;
+  // the split frequencies, [e][lane] so that a warp's reads are contiguous
+  __shared__ float2 s_fq[kM][32];
+  for (int i = threadIdx.x; i < HD / 2; i += kThreads) s_fq[i % kM][i / kM] = freq.f2[i];
   __syncthreads();
-  auto cu = [&](int i) { return staged ? s_cu[i] : cu_new[i]; };
-  const int total = cu(n_seqs);
+  const int lane = threadIdx.x & 31;
   const bool has_k = k != nullptr, has_v = v != nullptr;
-  const int nvec = n_q + (has_k ? n_kv : 0) + (has_v ? n_kv : 0);
+  // units of a token: q heads, then k heads, then v heads, NH at a time
+  const int uq = n_q / NH, uk = has_k ? n_kv / NH : 0, uv = has_v ? n_kv / NH : 0;
+  const int n_u = uq + uk + uv;
+  const int total = __ldg(cu_new + n_seqs);
+  if (total <= 0) return;
+  // this warp's units: a contiguous block, so that consecutive units mostly
+  // share a token (its position, slot and rotation are kept)
+  const int64_t n_units = static_cast<int64_t>(total) * n_u;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t per = (n_units + n_warps - 1) / n_warps;
+  const int64_t u0 = warp_id * per;
+  if (u0 >= n_units) return;
+  const int count = static_cast<int>(min(per, n_units - u0));
+  int t = static_cast<int>(u0 / n_u), g = static_cast<int>(u0 - (u0 / n_u) * n_u);
 
-  // loads of token t's head vectors warp, warp + WARPS, ... into r
-  auto load_rows = [&](int t, uint4 (&r)[ITEMS][kVecs]) {
+  // the sequence of the last token met: tokens [s_start, s_end)
+  int s_b = 0, s_start = 1, s_end = 0, s_past = 0;
+  int pos_t = -1, pos = 0;        // token whose position pos is known (-1: none)
+  int slot_t = -1;                // token whose page slot is known
+  int64_t slot = -1;
+  int rot_t = -1;                 // token whose rotation is in (rc, rs)
+  float rc[kM], rs[kM];
+
+  auto row_ptr = [&](int tt, int gg) -> const __nv_bfloat16* {
+    if (gg < uq) return q + (static_cast<int64_t>(tt) * n_q + gg * NH) * HD + lane * kM;
+    if (gg < uq + uk) return k + (static_cast<int64_t>(tt) * n_kv + (gg - uq) * NH) * HD + lane * kM;
+    return v + (static_cast<int64_t>(tt) * n_kv + (gg - uq - uk) * NH) * HD + lane * kM;
+  };
+  auto load = [&](int tt, int gg, Vec (&ra)[NH], Vec (&rb)[NH]) {
+    const __nv_bfloat16* src = row_ptr(tt, gg);
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      const int w = warp + u * WARPS;
-      if (w >= nvec) continue;  // uniform over the warp
-      const __nv_bfloat16* src;
-      if (w < n_q)
-        src = q + (static_cast<int64_t>(t) * n_q + w) * HD;
-      else if (has_k && w < n_q + n_kv)
-        src = k + (static_cast<int64_t>(t) * n_kv + (w - n_q)) * HD;
-      else
-        src = v + (static_cast<int64_t>(t) * n_kv + (w - n_q - (has_k ? n_kv : 0))) * HD;
-      const uint4* s4 = reinterpret_cast<const uint4*>(src) + lane * kVecs;
-#pragma unroll
-      for (int c = 0; c < kVecs; ++c) r[u][c] = s4[c];
+    for (int j = 0; j < NH; ++j) {
+      ra[j] = *reinterpret_cast<const Vec*>(src + j * HD);
+      rb[j] = *reinterpret_cast<const Vec*>(src + j * HD + HD / 2);
     }
   };
-  // sequence, position and slot of token t
-  auto resolve = [&](int t, int& pos_out, long long& slot_out) {
-    int lo = 0, hi = n_seqs;  // sequence owning token t: largest b with cu_new[b] <= t
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (cu(mid) <= t) lo = mid; else hi = mid;
+  // position of token tt; false: the token is skipped (flagged)
+  auto position = [&](int tt) -> bool {
+    if (tt == pos_t) return true;
+    if (!(tt >= s_start && tt < s_end)) {
+      if (!find_sequence(cu_new, past_lens, n_seqs, tt, lane, s_b, s_start, s_end, s_past)) {
+        if (lane == 0) flag_error(err, PSW_DEVERR_LENGTH);
+        s_start = 1;
+        s_end = 0;
+        return false;
+      }
     }
-    const int b = lo, start = cu(b);
-    int pos = -1;
-    long long slot = -1;
-    if (t < start || t >= cu(b + 1)) {
-      flag_error(err, PSW_DEVERR_LENGTH);  // offsets not monotone
-    } else {
-      const long long p = static_cast<long long>(past_lens[b]) + (t - start);
-      if (p < 0 || p > 0x7fffffffLL) {
-        flag_error(err, PSW_DEVERR_LENGTH);
+    const int64_t p = static_cast<int64_t>(s_past) + (tt - s_start);
+    if (s_past < 0 || p > 0x7fffffffLL) {
+      if (lane == 0) flag_error(err, PSW_DEVERR_LENGTH);
+      return false;
+    }
+    pos = static_cast<int>(p);
+    pos_t = tt;
+    return true;
+  };
+  // page slot of token tt (at position pos); false: no cache write (flagged)
+  auto page_slot = [&](int tt) -> bool {
+    if (tt != slot_t) {
+      slot_t = tt;
+      slot = -1;
+      const int page = pos / kBlockSize;
+      if (page >= max_blocks) {
+        if (lane == 0) flag_error(err, PSW_DEVERR_CAPACITY);
       } else {
-        pos = static_cast<int>(p);
-        if (has_k) {
-          const long long page = p / kBlockSize;
-          if (page >= max_blocks) {
-            flag_error(err, PSW_DEVERR_CAPACITY);
-          } else {
-            const int32_t blk = block_table[static_cast<int64_t>(b) * max_blocks + page];
-            if (blk < 0 || blk >= num_blocks)
-              flag_error(err, PSW_DEVERR_BLOCK_ID);
-            else
-              slot = static_cast<long long>(blk) * kBlockSize + p % kBlockSize;
-          }
+        const int32_t blk = __ldg(block_table + static_cast<int64_t>(s_b) * max_blocks + page);
+        if (blk < 0 || blk >= num_blocks) {
+          if (lane == 0) flag_error(err, PSW_DEVERR_BLOCK_ID);
+        } else {
+          slot = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
         }
       }
     }
-    pos_out = pos;
-    slot_out = slot;
+    return slot >= 0;
   };
-  // all threads: the rotation of stage st's token at position pos
-  auto angles = [&](TokenStage<HD>& st, int pos) {
-    for (int i = tid; i < kHalf; i += C::kThreads) {
-      float c = 1.f, sn = 0.f;
-      if (pos >= 0 && i < rope_angles) {
-        float r;
+  // rotation of this lane's pairs i = lane kM + e at position pos
+  auto rotation = [&](int tt) {
+    if (tt == rot_t) return;
+    rot_t = tt;
+#pragma unroll
+    for (int e = 0; e < kM; ++e) {
+      const int i = lane * kM + e;
+      float sn = 0.f, cs = 1.f;
+      if (i < rope_angles) {
+        float x;
+        int qd;
         if (pos < (1 << 24)) {
           // pos f = ph + pl from the float parts of f (pos is exact in a
-          // float, ph's rounding error comes back exactly from the FMA), then
-          // Cody-Waite reduction by the three-float 2 pi: each FMA multiplies
-          // exactly and rounds once, so |r - (pos f mod 2 pi)| stays below
-          // about 4e-7 for f <= 1
+          // float, ph's rounding error comes back exactly from the FMA),
+          // then Cody-Waite reduction by the three-float pi / 2: each FMA
+          // multiplies exactly and rounds once
+          const float2 fq = s_fq[e][lane];
           const float pf = static_cast<float>(pos);
-          const float2 fq = freq.f2[i];
           const float ph = pf * fq.x;
           const float pl = fmaf(pf, fq.y, fmaf(pf, fq.x, -ph));
-          const float n = rintf(ph * kInvTwoPi);
-          r = fmaf(-n, kC3, fmaf(-n, kC2, fmaf(-n, kC1, ph))) + pl;
+          const float n1 = rintf(ph * kTwoOverPi);
+          x = fmaf(-n1, kP3, fmaf(-n1, kP2, fmaf(-n1, kP1, ph))) + pl;
+          // above 2^22 the float products behind n1 (ph, ph 2/pi) can put
+          // it one or two off; x is still accurate for that n1, and a second
+          // reduction of x (a few pi / 2 at most, exact products) brings it
+          // back to [-pi/4, pi/4]
+          const float n2 = rintf(x * kTwoOverPi);
+          x = fmaf(-n2, kP2, fmaf(-n2, kP1, x));
+          qd = static_cast<int>(n1) + static_cast<int>(n2);
         } else {  // beyond 2^24 the product needs double
           const double a = static_cast<double>(pos) * freq.f[i];
-          const double n = rint(a * (1.0 / kTwoPiHi));
-          r = static_cast<float>(fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, a)));  // |r| <= pi
+          const double n1 = rint(a * (1.0 / kHalfPiHi));
+          x = static_cast<float>(fma(-n1, kHalfPiLo, fma(-n1, kHalfPiHi, a)));
+          qd = static_cast<int>(static_cast<int64_t>(n1) & 3);
         }
-        sincosf(r, &sn, &c);
+        sincos_quadrant(x, qd, sn, cs);
       }
-      st.cs[0][i] = make_float2(c, -sn);
-      st.cs[1][i] = make_float2(c, sn);
+      rc[e] = cs;
+      rs[e] = sn;
     }
   };
-  // every warp: normalise, rotate and store its vectors of token t
-  auto compute = [&](int t, const uint4 (&r)[ITEMS][kVecs], const TokenStage<HD>& st) {
-    if (st.pos < 0) return;
-    const long long slot = st.slot;
+  // normalise, rotate (q, k) and store the unit (tt, gg) held in (ra, rb)
+  auto process = [&](int tt, int gg, const Vec (&ra)[NH], const Vec (&rb)[NH]) {
+    if (!position(tt)) return;
+    const int kind = gg < uq ? 0 : (gg < uq + uk ? 1 : 2);
+    __nv_bfloat16* dst;
+    if (kind == 0) {
+      dst = q_out + (static_cast<int64_t>(tt) * n_q + gg * NH) * HD + lane * kM;
+    } else {
+      if (!page_slot(tt)) return;
+      const int h0 = (gg - (kind == 1 ? uq : uq + uk)) * NH;
+      dst = (kind == 1 ? k_pool : v_pool) + (slot * n_kv + h0) * HD + lane * kM;
+    }
+    const float* wt = kind == 0 ? qw : (kind == 1 ? kw : vw);
+    // per element coefficients: with the weights wa, wb and this lane's
+    // rotation (cos, sin) of pair lane kM + e,
+    //   out_a = inv (y_a wa cos - y_b wb sin), out_b = inv (y_b wb cos + y_a wa sin)
+    // and out = inv y w for v
+    float ca[kM], sa[kM], cb[kM], sb[kM];
 #pragma unroll
-    for (int u = 0; u < ITEMS; ++u) {
-      const int w = warp + u * WARPS;
-      if (w >= nvec) continue;  // uniform over the warp
-      __nv_bfloat16* dst;
-      const float* wt;
-      bool rot;
-      if (w < n_q) {
-        dst = q_out + (static_cast<int64_t>(t) * n_q + w) * HD;
-        wt = qw;
-        rot = true;
-      } else if (has_k && w < n_q + n_kv) {
-        dst = slot >= 0 ? k_pool + (slot * n_kv + (w - n_q)) * HD : nullptr;
-        wt = kw;
-        rot = true;
-      } else {
-        dst = slot >= 0 ? v_pool + (slot * n_kv + (w - n_q - (has_k ? n_kv : 0))) * HD
-                        : nullptr;
-        wt = vw;
-        rot = false;
-      }
-      if (dst == nullptr) continue;
-      float y[kPer];
-#pragma unroll
-      for (int c = 0; c < kVecs; ++c) {
-        const uint32_t wd[4] = {r[u][c].x, r[u][c].y, r[u][c].z, r[u][c].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          y[c * 8 + 2 * e] = __uint_as_float(wd[e] << 16);
-          y[c * 8 + 2 * e + 1] = __uint_as_float(wd[e] & 0xFFFF0000u);
-        }
-      }
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) ss = fmaf(y[e], y[e], ss);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      // MUFU reciprocal square root: about 2^-22 relative, far inside the
-      // error allowed before the bf16 rounding
-      const float inv = rsqrtf(ss * (1.f / HD) + eps);
+    for (int c4 = 0; c4 < kM / 4; ++c4) {
+      float4 a4 = make_float4(1.f, 1.f, 1.f, 1.f), b4 = a4;
       if (wt != nullptr) {
-        const float4* w4 = reinterpret_cast<const float4*>(wt) + lane * (kPer / 4);
+        a4 = __ldg(reinterpret_cast<const float4*>(wt + lane * kM) + c4);
+        b4 = __ldg(reinterpret_cast<const float4*>(wt + HD / 2 + lane * kM) + c4);
+      }
+      ca[4 * c4] = a4.x, ca[4 * c4 + 1] = a4.y, ca[4 * c4 + 2] = a4.z, ca[4 * c4 + 3] = a4.w;
+      cb[4 * c4] = b4.x, cb[4 * c4 + 1] = b4.y, cb[4 * c4 + 2] = b4.z, cb[4 * c4 + 3] = b4.w;
+    }
+    const bool rot = kind < 2;
+    if (rot) {
+      rotation(tt);
 #pragma unroll
-        for (int c = 0; c < kPer / 4; ++c) {
-          const float4 ww = __ldg(w4 + c);
-          y[4 * c] *= inv * ww.x;
-          y[4 * c + 1] *= inv * ww.y;
-          y[4 * c + 2] *= inv * ww.z;
-          y[4 * c + 3] *= inv * ww.w;
+      for (int e = 0; e < kM; ++e) {
+        sa[e] = ca[e] * rs[e];
+        ca[e] *= rc[e];
+        sb[e] = cb[e] * rs[e];
+        cb[e] *= rc[e];
+      }
+    }
+    // the sums of squares of the unit's rows, reduced together
+    float ss[NH];
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      float ya[kM], yb[kM];
+      S::unpack(ra[j], ya);
+      S::unpack(rb[j], yb);
+      ss[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < kM; ++e) ss[j] = fmaf(yb[e], yb[e], fmaf(ya[e], ya[e], ss[j]));
+    }
+    // MUFU reciprocal square root: about 2^-22 relative, far inside the
+    // error allowed before the bf16 rounding
+    const float inv_mine = rsqrtf(warp_sums<NH>(ss, lane) * (1.f / HD) + eps);
+#pragma unroll
+    for (int j = 0; j < NH; ++j) {
+      const float inv = __shfl_sync(0xffffffffu, inv_mine, j * (32 / NH));
+      float ya[kM], yb[kM], oa[kM], ob[kM];
+      S::unpack_again(ra[j], ya);
+      S::unpack_again(rb[j], yb);
+      if (rot) {
+#pragma unroll
+        for (int e = 0; e < kM; ++e) {
+          oa[e] = inv * fmaf(ya[e], ca[e], -(yb[e] * sb[e]));
+          ob[e] = inv * fmaf(yb[e], cb[e], ya[e] * sa[e]);
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) y[e] *= inv;
-      }
-      if (rot) {
-        const float4* cs4 =
-            reinterpret_cast<const float4*>(st.cs[lane >> 4] + (lane & 15) * kPer);
-#pragma unroll
-        for (int e2 = 0; e2 < kPer / 2; ++e2) {  // two pairs per 16-byte read
-          const float4 cc = cs4[e2];
-          const float o0 = __shfl_xor_sync(0xffffffffu, y[2 * e2], 16);
-          const float o1 = __shfl_xor_sync(0xffffffffu, y[2 * e2 + 1], 16);
-          y[2 * e2] = fmaf(y[2 * e2], cc.x, o0 * cc.y);
-          y[2 * e2 + 1] = fmaf(y[2 * e2 + 1], cc.z, o1 * cc.w);
+        for (int e = 0; e < kM; ++e) {
+          oa[e] = inv * (ya[e] * ca[e]);
+          ob[e] = inv * (yb[e] * cb[e]);
         }
       }
-      uint4* d4 = reinterpret_cast<uint4*>(dst) + lane * kVecs;
-#pragma unroll
-      for (int c = 0; c < kVecs; ++c)
-        d4[c] = make_uint4(pack_bf16_rn(y[c * 8], y[c * 8 + 1]),
-                           pack_bf16_rn(y[c * 8 + 2], y[c * 8 + 3]),
-                           pack_bf16_rn(y[c * 8 + 4], y[c * 8 + 5]),
-                           pack_bf16_rn(y[c * 8 + 6], y[c * 8 + 7]));
+      *reinterpret_cast<Vec*>(dst + j * HD) = S::pack(oa);
+      *reinterpret_cast<Vec*>(dst + j * HD + HD / 2) = S::pack(ob);
+    }
+  };
+  auto next = [&](int& tt, int& gg) {
+    if (++gg == n_u) {
+      gg = 0;
+      ++tt;
     }
   };
 
-  // This CTA's tokens are t = blockIdx.x + j * grid. Their positions and
-  // slots are resolved kNrChunk at a time, thread j taking token j, so no
-  // dependent lookup chain sits between two tokens. Tokens then run as a
-  // two-stage pipeline: while token j is computed, the rows of token j + 1
-  // are in flight; its angles are formed at the barrier between them. The
-  // loop is unrolled by two so that both row buffers stay in registers.
-  uint4 ra[ITEMS][kVecs], rb[ITEMS][kVecs];
-  const int G = static_cast<int>(gridDim.x);
-  const int n_mine = total > static_cast<int>(blockIdx.x)
-                         ? (total - static_cast<int>(blockIdx.x) + G - 1) / G
-                         : 0;
-  for (int c0 = 0; c0 < n_mine; c0 += kNrChunk) {
-    const int nc = min(kNrChunk, n_mine - c0);
-    auto tok = [&](int j) { return static_cast<int>(blockIdx.x) + (c0 + j) * G; };
-    load_rows(tok(0), ra);  // independent of every lookup
-    for (int j = tid; j < nc; j += C::kThreads) resolve(tok(j), s_poss[j], s_slots[j]);
-    __syncthreads();
-    s_st[0].pos = s_poss[0];
-    s_st[0].slot = s_slots[0];
-    angles(s_st[0], s_poss[0]);
-    __syncthreads();
-    for (int j = 0; j < nc;) {
-      // ---- token j from ra / stage 0, token j + 1 prepared into rb / stage 1
-      if (j + 1 < nc) load_rows(tok(j + 1), rb);
-      compute(tok(j), ra, s_st[0]);
-      if (++j >= nc) break;
-      if (tid == 0) { s_st[1].pos = s_poss[j]; s_st[1].slot = s_slots[j]; }
-      angles(s_st[1], s_poss[j]);
-      __syncthreads();
-      // ---- token j from rb / stage 1, token j + 1 prepared into ra / stage 0
-      if (j + 1 < nc) load_rows(tok(j + 1), ra);
-      compute(tok(j), rb, s_st[1]);
-      if (++j >= nc) break;
-      if (tid == 0) { s_st[0].pos = s_poss[j]; s_st[0].slot = s_slots[j]; }
-      angles(s_st[0], s_poss[j]);
-      __syncthreads();
-    }
-    __syncthreads();  // the chunk arrays are rewritten by the next chunk
+  // two register buffers: the next unit's rows are in flight while one is
+  // processed
+  Vec a0[NH], b0[NH], a1[NH], b1[NH];
+  load(t, g, a0, b0);
+  for (int c = 0; c < count; c += 2) {
+    int t1 = t, g1 = g;
+    next(t1, g1);
+    if (c + 1 < count) load(t1, g1, a1, b1);
+    process(t, g, a0, b0);
+    if (c + 1 >= count) break;
+    int t2 = t1, g2 = g1;
+    next(t2, g2);
+    if (c + 2 < count) load(t2, g2, a0, b0);
+    process(t1, g1, a1, b1);
+    t = t2;
+    g = g2;
   }
 }
 
-template <int HD, int WARPS>
-cudaError_t launch_items(int items, const FreqTable& ft, int grid, cudaStream_t stream,
-                         const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
-                         const int32_t* cu_new, const int32_t* past_lens, int n_seqs,
-                         const int32_t* block_table, int max_blocks, int64_t num_blocks, int n_q,
-                         int n_kv, float eps, const float* qw, const float* kw, const float* vw,
-                         int rope_angles, __nv_bfloat16* qo, __nv_bfloat16* kp,
-                         __nv_bfloat16* vp, int32_t* err) {
-#define PSW_NR_LAUNCH(I)                                                                      \
-  qkv_norm_rope_kernel<HD, WARPS, I><<<grid, WARPS * 32, 0, stream>>>(                        \
-      ft, q, k, v, cu_new, past_lens, n_seqs, block_table, max_blocks, num_blocks, n_q, n_kv, \
-      eps, qw, kw, vw, rope_angles, qo, kp, vp, err)
-  if (items <= 1) PSW_NR_LAUNCH(1);
-  else if (items <= 2) PSW_NR_LAUNCH(2);
-  else if (items <= 3) PSW_NR_LAUNCH(3);
-  else PSW_NR_LAUNCH(4);
-#undef PSW_NR_LAUNCH
-  return cudaGetLastError();
+// CTAs resident on an SM (registers decide it), asked once: the grid is
+// that many per SM, so every CTA is resident from the start.
+template <int HD, int NH>
+int resident_ctas() {
+  static std::atomic<int> cached{0};
+  int n = cached.load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qkv_norm_rope_kernel<HD, NH>, kThreads,
+                                                      0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    cached.store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 }  // namespace
@@ -353,29 +488,31 @@ int launch_qkv_norm_rope(const LayerArgs& L, const NormRopeArgs& R, const void* 
     const float hi = static_cast<float>(ft.f[i]);
     ft.f2[i] = make_float2(hi, static_cast<float>(ft.f[i] - static_cast<double>(hi)));
   }
-  const int nvec = L.n_q + (k != nullptr ? L.n_kv : 0) + (v != nullptr ? L.n_kv : 0);
-  // 8 warps (16 at head_dim 512), each holding up to 4 head vectors of a
-  // token per stage
-  const int warps = L.hd == 256 ? 8 : 16;
-  const int items = (nvec + warps - 1) / warps;
-  if (items > 4) return PSW_EINVAL_HEADS;
-  const int grid = num_sms * (L.hd == 256 ? 3 : 2);  // about one wave of resident CTAs
   const auto* qb = static_cast<const __nv_bfloat16*>(q);
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
   auto* qo = static_cast<__nv_bfloat16*>(q_out);
   auto* kp = static_cast<__nv_bfloat16*>(k_pool);
   auto* vp = static_cast<__nv_bfloat16*>(v_pool);
-  const cudaError_t e =
-      L.hd == 256
-          ? launch_items<256, 8>(items, ft, grid, stream, qb, kb, vb, cu_new, past_lens, n_seqs,
-                                 block_table, max_blocks, num_blocks, L.n_q, L.n_kv, R.eps,
-                                 R.q_weight, R.k_weight, R.v_weight, R.rope_angles, qo, kp, vp,
-                                 err)
-          : launch_items<512, 16>(items, ft, grid, stream, qb, kb, vb, cu_new, past_lens, n_seqs,
-                                  block_table, max_blocks, num_blocks, L.n_q, L.n_kv, R.eps,
-                                  R.q_weight, R.k_weight, R.v_weight, R.rope_angles, qo, kp, vp,
-                                  err);
+  // head vectors per unit: the largest of 4, 2, 1 dividing the head counts
+  // at head_dim 256, 1 at 512 (two units of rows per warp stay within its
+  // registers)
+  const bool kv = k != nullptr || v != nullptr;
+  int nh = L.hd == 256 ? 4 : 1;
+  while (nh > 1 && (L.n_q % nh != 0 || (kv && L.n_kv % nh != 0))) nh >>= 1;
+#define PSW_NR_LAUNCH(HD_, NH_)                                                             \
+  qkv_norm_rope_kernel<HD_, NH_><<<num_sms * resident_ctas<HD_, NH_>(), kThreads, 0, stream>>>( \
+      ft, qb, kb, vb, cu_new, past_lens, n_seqs, block_table, max_blocks, num_blocks, L.n_q,  \
+      L.n_kv, R.eps, R.q_weight, R.k_weight, R.v_weight, R.rope_angles, qo, kp, vp, err)
+  if (L.hd == 256) {
+    if (nh == 4) PSW_NR_LAUNCH(256, 4);
+    else if (nh == 2) PSW_NR_LAUNCH(256, 2);
+    else PSW_NR_LAUNCH(256, 1);
+  } else {
+    PSW_NR_LAUNCH(512, 1);
+  }
+#undef PSW_NR_LAUNCH
+  const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PSW_OK : PSW_ELAUNCH;
 }
 

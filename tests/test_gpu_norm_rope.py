@@ -106,6 +106,35 @@ def test_norm_rope_large_positions(orc):
     run_case(orc, NormRopeCase(orc, layer, [65530, 69000, 40000], [8, 1, 3], 104, 1e6, 1.0))
 
 
+@pytest.mark.parametrize("hd,theta,factor", [(256, 1e4, 1.0), (512, 1e6, 0.25)])
+def test_norm_rope_positions_past_2_22(orc, hd, theta, factor):
+    """q-only calls (no cache write, so no pages) at positions where the
+    float angle reduction takes its second step (2^22 to 2^24), across the
+    switch to double at 2^24, and on to 2^26 (where the oracle's own fp64
+    product is still good to about 1.5e-8 rad)."""
+    layer = Layer(8, 4, hd, window=0)
+    rng = np.random.default_rng(108)
+    past = np.array([2**22 - 5, 2**23 + 11, 2**24 - 4, 2**24 + 1, 2**25 + 3, 2**26 - 9],
+                    np.int32)
+    new = np.array([9, 3, 8, 2, 4, 7], np.int32)
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    n = int(cu[-1])
+    q_raw = wl.f32_to_bf16_bits((3.0 * rng.standard_normal((n, 8, hd))).astype(np.float32))
+    qw = (1.0 + 0.1 * rng.standard_normal(hd)).astype(np.float32)
+    angles = int(factor * hd / 2)
+    exact = orc.qkv_norm_rope(q_raw, None, None, cu, past, 1e-6, theta, angles, q_w=qw)[0]
+    pre = orc.qkv_norm_rope(q_raw, None, None, cu, past, 1e-6, theta, 0, q_w=qw)[0]
+    w_dev = torch.from_numpy(qw).cuda()
+    rn = binding.make_norm_rope(theta, factor, 1e-6, w_dev, None, None)
+    q = dev_bf16(q_raw)
+    out = torch.empty_like(q)
+    binding.qkv_norm_rope_cache_write(layer, rn, q, None, None, torch.from_numpy(cu).cuda(),
+                                      torch.from_numpy(past).cuda(), None, out, None, None)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert_norm_rope_close(host_bits(out), exact, pre, True, f"q_out hd {hd}")
+
+
 def test_norm_rope_q_only_leaves_pools(orc):
     """A layer reading another layer's cache: only q is processed, in place,
     and no pool changes."""
