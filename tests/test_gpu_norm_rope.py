@@ -106,6 +106,21 @@ def test_norm_rope_large_positions(orc):
     run_case(orc, NormRopeCase(orc, layer, [65530, 69000, 40000], [8, 1, 3], 104, 1e6, 1.0))
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(4, 2), (3, 1)])
+def test_norm_rope_many_sequences_with_empty_chunks(orc, n_q, n_kv):
+    """1100 sequences (the warp's sequence search takes three rounds past 961)
+    with new lengths 0, 1, 2 or 5 and pasts across page boundaries: every
+    token lands in its own sequence's slot, empty sequences write nothing.
+    Few KV heads keep the pools small; the head counts give units of two
+    head vectors and of one."""
+    layer = Layer(n_q, n_kv, 256, window=1024)
+    rng = np.random.default_rng(109)
+    n = 1100
+    new = rng.choice([0, 0, 1, 2, 5], size=n)
+    past = rng.integers(0, 40, size=n)
+    run_case(orc, NormRopeCase(orc, layer, past, new, 110, 1e4, 1.0))
+
+
 @pytest.mark.parametrize("hd,theta,factor", [(256, 1e4, 1.0), (512, 1e6, 0.25)])
 def test_norm_rope_positions_past_2_22(orc, hd, theta, factor):
     """q-only calls (no cache write, so no pages) at positions where the
