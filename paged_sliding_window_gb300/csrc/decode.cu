@@ -572,23 +572,33 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
     const uint32_t kbase = FP8 ? smem_u32(conv) : stages_u32 + stage * C::kStageBytes;
     const uint32_t vbase = KEQV ? kbase : kbase + C::kKTileBytes;
 
-    // ---- QK over this warp's quarter of head_dim: S^T[key, qh]
+    // ---- QK over this warp's quarter of head_dim: S^T[key, qh]. Even and
+    // odd head_dim steps go to two accumulators (two independent MMA chains
+    // per page instead of one), added at the end.
     float sacc[TP][4];
-    #pragma unroll
-    for (int mt = 0; mt < TP; ++mt) {
-      sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+    if (landed) {
+      float sacc2[TP][4];
       #pragma unroll
-      for (int ks = 0; ks < C::kKSteps; ++ks) {
-        if (!landed) break;
-        const int d0 = warp * C::kDPerWarp + ks * 16;
-        const int c = d0 >> 6;
-        const int u = ((d0 & 63) >> 3) + qk_unit_add;
-        const uint32_t addr = kbase + mt * C::kPageBytes + c * kChunkBytes + qk_row * 128 +
-                              ((u ^ (qk_row & 7)) << 4);
-        uint32_t a[4];
-        ldsm_x4(addr, a);
-        mma_bf16_16816(sacc[mt], a, qf[ks][0], qf[ks][1]);
+      for (int mt = 0; mt < TP; ++mt) {
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][e] = sacc2[mt][e] = 0.f;
+        #pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          const int d0 = warp * C::kDPerWarp + ks * 16;
+          const int c = d0 >> 6;
+          const int u = ((d0 & 63) >> 3) + qk_unit_add;
+          const uint32_t addr = kbase + mt * C::kPageBytes + c * kChunkBytes + qk_row * 128 +
+                                ((u ^ (qk_row & 7)) << 4);
+          uint32_t a[4];
+          ldsm_x4(addr, a);
+          mma_bf16_16816((ks & 1) ? sacc2[mt] : sacc[mt], a, qf[ks][0], qf[ks][1]);
+        }
+        #pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][e] += sacc2[mt][e];
       }
+    } else {
+      #pragma unroll
+      for (int mt = 0; mt < TP; ++mt) sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
     }
     float* sb = sbuf + (consumed & 1) * C::kSBufFloats;
     {
@@ -696,15 +706,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
       }
     }
 
-    // ---- rescale O^T and accumulate PV over this warp's quarter
-    const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t4) * 4);
-    const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t4 + 1) * 4);
-    #pragma unroll
-    for (int mt2 = 0; mt2 < C::kMTiles; ++mt2) {
-      o[mt2][0] *= a0;
-      o[mt2][1] *= a1;
-      o[mt2][2] *= a0;
-      o[mt2][3] *= a1;
+    // ---- rescale O^T (only when some query head's maximum rose: alpha is
+    // exactly 1 otherwise) and accumulate PV over this warp's quarter
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t4) * 4);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t4 + 1) * 4);
+      #pragma unroll
+      for (int mt2 = 0; mt2 < C::kMTiles; ++mt2) {
+        o[mt2][0] *= a0;
+        o[mt2][1] *= a1;
+        o[mt2][2] *= a0;
+        o[mt2][3] *= a1;
+      }
     }
     #pragma unroll
     for (int kk = 0; kk < TP; ++kk) {
