@@ -178,6 +178,57 @@ def test_norm_rope_bad_block_is_flagged_q_still_written(orc):
     _check_q(case, host_bits(out))
 
 
+def test_norm_rope_bad_lengths_are_flagged(orc):
+    """A sequence with a negative past length is skipped whole (flagged as a
+    length error: no q_out row, no cache write); a sequence past the end of
+    its block-table row still gets its q_out rows at their positions, only
+    its K/V rows are dropped (a capacity error). The third sequence is
+    processed as usual, and no other pool slot changes."""
+    layer = Layer(8, 4, 256, window=1024)
+    case = NormRopeCase(orc, layer, [10, 20, 30], [2, 3, 2], 111, 1e4, 1.0)
+    st = case.step
+    g = GpuStep(st)
+    k_before, v_before = host_bits(g.k_pool), host_bits(g.v_pool)
+    max_blocks = int(g.table.shape[1])
+    past = st.past_lens.astype(np.int32).copy()
+    past[1] = -7                   # every token of sequence 1 at a negative position
+    past[2] = max_blocks * 16      # sequence 2 beyond its block-table row
+    g.past = torch.from_numpy(past).cuda()
+    nan_bits = 0x7FC0
+    out = torch.from_numpy(np.full(case.q_raw.shape, nan_bits, np.uint16).view(np.int16)).cuda()
+    out = out.view(torch.bfloat16)
+    case.gpu(g, q_out=out)
+    torch.cuda.synchronize()
+    err = binding.get_error()
+    assert err & binding.DEVERR_LENGTH and err & binding.DEVERR_CAPACITY, err
+    got = host_bits(out)
+    cu = st.cu_new.astype(np.int32)
+    past_ok = past.copy()
+    past_ok[1] = 0  # the oracle needs some position; those rows are not compared
+    exact = orc.qkv_norm_rope(case.q_raw, None, None, cu, past_ok, case.eps, case.theta,
+                              case.rope_angles, q_w=case.qw)[0]
+    pre = orc.qkv_norm_rope(case.q_raw, None, None, cu, past_ok, case.eps, case.theta, 0,
+                            q_w=case.qw)[0]
+    for b in (0, 2):
+        rows = slice(int(cu[b]), int(cu[b + 1]))
+        assert_norm_rope_close(got[rows], exact[rows], pre[rows], True, f"q_out of sequence {b}")
+    assert np.all(got[int(cu[1]):int(cu[2])] == nan_bits), "a skipped token's q_out row was written"
+    # pools: only sequence 0's slots change
+    _, ek, ev = case.oracle_exact()
+    _, pk, pv = case.oracle_exact(rotate=False)
+    n0 = int(cu[1])
+    slots = [(int(st.block_table[0, (int(st.past_lens[0]) + i) // 16]), (int(st.past_lens[0]) + i) % 16)
+             for i in range(n0)]
+    idx = tuple(np.array(slots).T)
+    for pool, before, ex, pr, rot, what in ((g.k_pool, k_before, ek, pk, True, "K"),
+                                           (g.v_pool, v_before, ev, pv, False, "V")):
+        bits = host_bits(pool)
+        assert_norm_rope_close(bits[idx], ex[:n0], pr[:n0], rot, f"{what} rows of sequence 0")
+        mask = np.ones(bits.shape[:2], bool)
+        mask[idx] = False
+        assert np.array_equal(bits[mask], before[mask]), f"{what}: a slot outside sequence 0 changed"
+
+
 @pytest.mark.parametrize("mode", ["decode", "prefill"])
 def test_fused_step_then_attention_matches_oracle_pipeline(orc, mode):
     """The layer path from raw projections: fused step, then decode or chunked
