@@ -266,6 +266,11 @@ def test_norm_rope_argument_checks(lib):
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="host without a GPU only")
 def test_norm_rope_without_gpu_fails_loudly(lib):
     assert _norm_rope(lib, _layer()) == -13
+    # any number of heads per token passes the argument checks (the kernel
+    # takes a token's head vectors a few at a time): it reaches the device
+    # step, which has no GPU here
+    assert _norm_rope(lib, _layer(n_q_heads=128, n_kv_heads=16)) == -13
+    assert _norm_rope(lib, _layer(n_q_heads=96, n_kv_heads=8, head_dim=512, window=0)) == -13
 
 
 def _decode8(lib, layer, q=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, pages=None, seq=FAKE, n=4,

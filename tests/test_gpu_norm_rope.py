@@ -82,6 +82,14 @@ def test_norm_rope_sliding_layer(orc):
     run_case(orc, NormRopeCase(orc, layer, past, new, 101, 1e4, 1.0))
 
 
+def test_norm_rope_many_heads(orc):
+    """48 query and 16 KV heads (80 head vectors per token, more than one
+    warp's share in the earlier layout): units of four head vectors, twelve
+    of q and four each of k and v per token."""
+    layer = Layer(48, 16, 256, window=1024)
+    run_case(orc, NormRopeCase(orc, layer, [5, 100, 0], [3, 17, 1], 112, 1e4, 1.0))
+
+
 def test_norm_rope_full_layer_partial_k_eq_v(orc):
     """Full layer (head_dim 512, theta 1e6, a quarter of the dims rotated), V
     aliasing the K pages: only K is written."""
